@@ -1,0 +1,559 @@
+#!/usr/bin/env python
+"""Paged decode attention benchmark: µs per batch and KV GB/s vs HBM peak.
+
+One step = one pass of the whole hot path over one synthetic batch: plan on
+the host (lengths -> split-KV work list -> H2D copy of the plan image), the
+decode kernel, and the split-KV merge kernel.  The default workload is the
+64-request batch (lengths uniform on [128, 4096], Hq 32 / Hkv 8, head_dim 128,
+page_size 16, fp16); ``--workload`` selects another of
+paged_kv_decode_plan_gb300.workloads.
+
+Rank 0 prints one JSON line.  Under torchrun every rank runs the same batch
+on its own GPU (weak scaling, no data-path collective); timing is the maximum
+over ranks.  ``--impl reference`` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("paged decode attention µs/batch and KV GB/s as fraction of "
+          "GB300 HBM peak")
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+DESCRIPTIONS = {
+    "single": "single-request decode: 1 x 512 tokens, Hq 32 / Hkv 8, D 128, P 16, fp16",
+    "batch64": "batch 64 decode: lengths U[128,4096], Hq 32 / Hkv 8, D 128, P 16, fp16",
+    "longtail": "batch 256 long-tail decode: lengths logN(ln 1024, 1) in [16, 32768], "
+                "Hq 32 / Hkv 8, D 128, P 1, bf16",
+    "cascade": "cascade: 128 x (8192 shared prefix stored once + U[64,1024] suffix), "
+               "Hq 32 / Hkv 8, D 128, P 16, fp16",
+    "longctx": "long-context decode: 8 x 131072 tokens, Hq 64 / Hkv 8, D 128, P 64, bf16, "
+               ">=132 partitions per request",
+}
+KERNEL_SOURCES = ["paged_kv_decode_plan_gb300/csrc/decode.cu",
+                  "paged_kv_decode_plan_gb300/csrc/ptx.cuh"]
+
+
+# ----------------------------------------------------------------- ranks
+
+class Ranks:
+    """Rank bookkeeping; a single process when WORLD_SIZE is unset."""
+
+    def __init__(self, backend=None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend or "nccl")
+            self.dist = dist
+        self.backend = backend or "nccl"
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def reduce_max(self, x: float) -> float:
+        if self.dist is None:
+            return x
+        import torch
+        dev = "cuda" if self.backend == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def reduce_sum(self, x: float) -> float:
+        if self.dist is None:
+            return x
+        import torch
+        dev = "cuda" if self.backend == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+def aggregate(ranks: Ranks, per_rank_bytes: float, elapsed_s: float, steps: int):
+    """Whole-job throughput: all ranks' bytes over the slowest rank's time."""
+    total_bytes = ranks.reduce_sum(per_rank_bytes)
+    slowest = ranks.reduce_max(elapsed_s)
+    return {"value_gbs": total_bytes * steps / slowest / 1e9,
+            "ms_per_step": slowest * 1e3 / steps, "slowest_s": slowest}
+
+
+# ----------------------------------------------------------------- helpers
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if the
+    summary was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_%s_ncu.txt" % workload)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+        self.window = [None, None]
+
+    def mark(self, which: int):
+        """Records the sample-file offset at the start (0) / end (1) of load."""
+        time.sleep(0.15 if which else 0.0)
+        self.window[which] = os.path.getsize(self.path)
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader",
+                 "-lms", "100"], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                f.seek(self.window[0] or 0)
+                text = f.read((self.window[1] or 1 << 30) - (self.window[0] or 0))
+            for line in text.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and self.uuid not in parts[1]:
+                    continue
+                try:
+                    rows.append((float(parts[2].split()[0]), float(parts[3].split()[0]),
+                                 parts[6:10]))
+                except ValueError:
+                    continue
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows
+                          for i, f in enumerate(flags) if f.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- our arm
+
+class Runner:
+    """Device-resident batch plus workspaces; one `step()` = plan + run."""
+
+    def __init__(self, wl, device):
+        import torch
+        import paged_kv_decode_plan_gb300 as pkd
+        self.pkd = pkd
+        self.wl = wl
+        self.device = device
+        self.q = wl.q.to(device)
+        self.k = wl.k_pages.to(device)
+        self.v = wl.v_pages.to(device)
+        self.tables = ([wl.extra_tables["prefix"], wl.extra_tables["suffix"]]
+                       if wl.name == "cascade" else [wl.table])
+        self.parts = []
+        for t in self.tables:
+            prob = pkd.make_problem(batch=t.batch, num_qo_heads=wl.num_qo_heads,
+                                    num_kv_heads=wl.num_kv_heads, page_size=t.page_size,
+                                    dtype=wl.dtype, num_pages=wl.num_pages,
+                                    min_chunks_per_request=wl.min_chunks_per_request)
+            ws = pkd.Workspace(prob, device=device)
+            dev = tuple(torch.from_numpy(a).to(device) for a in
+                        (t.kv_indptr, t.kv_indices, t.kv_last_page_len))
+            out = torch.empty_like(self.q)
+            lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
+            self.parts.append(dict(table=t, ws=ws, dev=dev, out=out, lse=lse))
+        self.final = (torch.empty_like(self.q),
+                      torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
+        self.launches_per_step = 0
+
+    def step(self, dec_events=None):
+        launches = 0
+        for part in self.parts:
+            t = part["table"]
+            plan = part["ws"].plan(t.kv_indptr, t.kv_last_page_len, None)
+            part["plan"] = plan
+            if dec_events is not None:
+                dec_events[0].record()
+            part["ws"].run(plan, self.q, self.k, self.v, *part["dev"], self.wl.sm_scale,
+                           out=part["out"], lse=part["lse"], phase="decode")
+            if dec_events is not None:
+                dec_events[1].record()
+                dec_events = None   # time the first (largest) decode launch
+            part["ws"].run(plan, self.q, self.k, self.v, *part["dev"], self.wl.sm_scale,
+                           out=part["out"], lse=part["lse"], phase="merge")
+            launches += 1 + (plan.num_split_requests > 0)
+        if len(self.parts) == 2:
+            a, b = self.parts
+            self.pkd.merge_states(a["out"], a["lse"], b["out"], b["lse"],
+                                  v_out=self.final[0], s_out=self.final[1])
+            launches += 1
+        self.launches_per_step = launches
+
+    def kv_bytes(self):
+        """Algorithmic KV bytes per step (a shared prefix counted once)."""
+        wl = self.wl
+        per_token = 2 * wl.num_kv_heads * wl.head_dim * wl.k_pages.element_size()
+        if wl.name == "cascade":
+            prefix = wl.extra_tables["prefix"]
+            prefix_tokens = int(prefix.lengths()[0]) if prefix.batch else 0
+            return (prefix_tokens + int(wl.extra_tables["suffix"].lengths().sum())) * per_token
+        return int(wl.table.lengths().sum()) * per_token
+
+    def decode_kv_bytes(self):
+        """KV bytes the timed decode launch reads (first table)."""
+        wl = self.wl
+        per_token = 2 * wl.num_kv_heads * wl.head_dim * wl.k_pages.element_size()
+        return int(self.tables[0].lengths().sum()) * per_token
+
+
+def run_ours(args, ranks):
+    import torch
+    from paged_kv_decode_plan_gb300 import workloads
+
+    torch.cuda.set_device(ranks.local)
+    device = torch.device("cuda", ranks.local)
+    wl = workloads.WORKLOADS[args.workload]()
+    runner = Runner(wl, device)
+    stream = torch.cuda.current_stream()
+
+    # host plan time (median of 20)
+    part = runner.parts[0]
+    problem = _explicit(part["ws"].problem, runner)
+    plan_times = []
+    for _ in range(20):
+        t0 = time.perf_counter()
+        runner.pkd.plan_host(problem, part["table"].kv_indptr,
+                             part["table"].kv_last_page_len)
+        plan_times.append(time.perf_counter() - t0)
+
+    for _ in range(args.warmup):
+        runner.step()
+    torch.cuda.synchronize()
+    status = runner.pkd.check_status(part["ws"].int_ws)
+    if status:
+        raise RuntimeError("device status word %d after warm-up" % status)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:  # noqa: BLE001 - older torch
+        uuid = None
+    k = args.steps
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(k)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clocks:
+        ranks.barrier()
+        torch.cuda.synchronize()
+        clocks.mark(0)
+        start.record(stream)
+        for i in range(k):
+            runner.step(events[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        ranks.barrier()
+        # end to end through the public API with host buffers
+        e2e = run_e2e(args, runner, device, ranks)
+        clocks.mark(1)
+    elapsed = start.elapsed_time(end) / 1e3
+    decode_ms = [a.elapsed_time(b) for a, b in events]
+    agg = aggregate(ranks, runner.kv_bytes(), elapsed, k)
+    decode_mean_ms = ranks.reduce_max(statistics.fmean(decode_ms))
+
+    peak, peak_kind = load_peak()
+    achieved = runner.decode_kv_bytes() / (decode_mean_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(agg["value_gbs"], 2), "unit": "GB/s",
+        "n_gpus": ranks.world, "steps": k, "warmup": args.warmup,
+        "ms_per_step": round(agg["ms_per_step"], 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "accumulate": "f32",
+        "data": "synthetic (seeded N(0,1), shapes of the workload)",
+        "config": {"workload": DESCRIPTIONS[wl.name], "name": wl.name,
+                   "batch": wl.batch, "num_qo_heads": wl.num_qo_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "page_size": wl.page_size, "kv_bytes_per_step": runner.kv_bytes(),
+                   "l2": ("inputs larger than L2 (KV %.0f MB vs 129 MB), no flush"
+                          % (runner.kv_bytes() / 1e6)) if runner.kv_bytes() > 2 * L2_BYTES
+                   else "KV fits in L2: warm-L2 number",
+                   "parallelism": "replicas (weak scaling, no collective)"},
+        "us_per_batch": round(agg["ms_per_step"] * 1e3, 2),
+        "hbm_frac_of_%s" % peak_kind: round(agg["value_gbs"] / ranks.world / peak, 4),
+        "decode_us": round(decode_mean_ms * 1e3, 2),
+        "plan_host_us": round(statistics.median(plan_times) * 1e6, 1),
+        "num_units": runner.parts[0]["plan"].num_units,
+        "num_split_requests": runner.parts[0]["plan"].num_split_requests,
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel",
+                     "achieved": round(achieved, 2), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(wl.name),
+                     "algorithmic_bytes_per_launch": runner.decode_kv_bytes()},
+        "e2e": e2e,
+        "gpu_launches": runner.launches_per_step * k,
+        "clocks": clocks.summary(),
+    }
+    if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+    return line
+
+
+def _explicit(problem, runner):
+    import paged_kv_decode_plan_gb300 as pkd
+    p = pkd.Problem.from_buffer_copy(problem)
+    if p.num_ctas <= 0:
+        import torch
+        p.num_ctas = torch.cuda.get_device_properties(runner.device).multi_processor_count
+    return p
+
+
+def run_e2e(args, runner, device, ranks):
+    """Same metric through the public API: H2D of the step's inputs (queries
+    and page table) from pinned memory, plan, run, D2H of out and lse."""
+    import torch
+    wl = runner.wl
+    q_h = wl.q.pin_memory()
+    tables_h = [tuple(torch.from_numpy(a).pin_memory() for a in
+                      (p["table"].kv_indptr, p["table"].kv_indices,
+                       p["table"].kv_last_page_len)) for p in runner.parts]
+    out_h = torch.empty(runner.q.shape, dtype=runner.q.dtype, pin_memory=True)
+    lse_h = torch.empty(runner.q.shape[:2], dtype=torch.float32, pin_memory=True)
+    h2d = q_h.numel() * q_h.element_size() + sum(
+        sum(t.numel() * 4 for t in th) for th in tables_h)
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def one():
+        runner.q.copy_(q_h, non_blocking=True)
+        for part, th in zip(runner.parts, tables_h):
+            for dst, src in zip(part["dev"], th):
+                dst.copy_(src, non_blocking=True)
+        runner.step()
+        res = runner.final if len(runner.parts) == 2 else (runner.parts[0]["out"],
+                                                           runner.parts[0]["lse"])
+        out_h.copy_(res[0], non_blocking=True)
+        lse_h.copy_(res[1], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        one()
+    image_bytes = sum(int(p["plan"].int_ws_bytes_used) for p in runner.parts)
+    ranks.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    elapsed = time.perf_counter() - t0
+    agg = aggregate(ranks, runner.kv_bytes(), elapsed, steps)
+    return {"value": round(agg["value_gbs"], 2), "unit": "GB/s",
+            "us_per_batch": round(agg["ms_per_step"] * 1e3, 2), "steps": steps,
+            "h2d_bytes_per_step": h2d + image_bytes, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------- oracle arm
+
+def _oracle_rows_for(wl, first_req, n_req):
+    hq = wl.num_qo_heads
+    return np.arange(first_req * hq, (first_req + n_req) * hq, dtype=np.int64)
+
+
+def cpu_baseline(wl, budget_s: float, kind="oracle"):
+    """Times the fp64 oracle on whole requests of the workload (in batch order,
+    wrapping around) until about budget_s of wall time has passed."""
+    import oracle
+    from paged_kv_decode_plan_gb300 import workloads
+    codes = (workloads.as_codes(wl.q), workloads.as_codes(wl.k_pages),
+             workloads.as_codes(wl.v_pages))
+    t = wl.table
+    lengths = t.lengths()
+    per_token = 2 * wl.num_kv_heads * wl.head_dim * wl.k_pages.element_size()
+    done_bytes = 0
+    done_req = 0
+    elapsed = 0.0
+    b = 0
+    while elapsed < budget_s and done_req < 4 * wl.batch:
+        rows = _oracle_rows_for(wl, b, 1)
+        t0 = time.perf_counter()
+        oracle.decode(*codes, t.kv_indptr, t.kv_indices, t.kv_last_page_len,
+                      dtype=wl.dtype, sm_scale=wl.sm_scale, rows=rows)
+        elapsed += time.perf_counter() - t0
+        done_bytes += int(lengths[b]) * per_token
+        done_req += 1
+        b = (b + 1) % wl.batch
+    gbs = done_bytes / elapsed / 1e9 if elapsed > 0 else 0.0
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": kind, "seconds": round(elapsed, 2),
+            "us_per_batch_equiv": round(elapsed / max(done_bytes, 1) *
+                                        sum(int(x) for x in lengths) * per_token * 1e6, 1),
+            "sample": "%d whole requests (all %d query heads each) of the %s workload, "
+                      "fp64 page-table walk" % (done_req, wl.num_qo_heads, wl.name)}
+
+
+def run_reference(args, ranks):
+    """The oracle as it stands, on the host cores, same metric and config."""
+    import oracle
+    from paged_kv_decode_plan_gb300 import workloads
+    oracle.build()
+    wl = workloads.WORKLOADS[args.workload]()
+    codes = (workloads.as_codes(wl.q), workloads.as_codes(wl.k_pages),
+             workloads.as_codes(wl.v_pages))
+    t = wl.table
+    lengths = t.lengths()
+    per_token = 2 * wl.num_kv_heads * wl.head_dim * wl.k_pages.element_size()
+    hq = wl.num_qo_heads
+    # calibrate: rows per step so that warm-up + steps take about budget_s
+    t0 = time.perf_counter()
+    oracle.decode(*codes, t.kv_indptr, t.kv_indices, t.kv_last_page_len,
+                  dtype=wl.dtype, sm_scale=wl.sm_scale, rows=np.arange(hq))
+    per_req = max(time.perf_counter() - t0, 1e-4)
+    per_step = args.reference_budget_s / max(1, args.steps + args.warmup)
+    rows_per_step = int(max(1, min(wl.batch * hq, per_step / per_req * hq)))
+    cursor = [0]
+
+    def step():
+        total = wl.batch * hq
+        rows = (np.arange(rows_per_step, dtype=np.int64) + cursor[0]) % total
+        cursor[0] = (cursor[0] + rows_per_step) % total
+        oracle.decode(*codes, t.kv_indptr, t.kv_indices, t.kv_last_page_len,
+                      dtype=wl.dtype, sm_scale=wl.sm_scale, rows=rows)
+        return sum(int(lengths[r // hq]) for r in rows) * per_token / hq
+
+    for _ in range(args.warmup):
+        step()
+    done = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        done += step()
+    elapsed = time.perf_counter() - t0
+    gbs = done / elapsed / 1e9
+    sample = ("%d (request, query-head) rows per step of the %s workload, fp64 "
+              "page-table walk" % (rows_per_step, wl.name))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), shapes of the workload)",
+        "config": {"workload": DESCRIPTIONS[wl.name], "name": wl.name,
+                   "batch": wl.batch, "num_qo_heads": hq,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "page_size": wl.page_size},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s",
+                         "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(DESCRIPTIONS), default="batch64")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--reference-budget-s", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        line = run_reference(args, _single_rank())
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import paged_kv_decode_plan_gb300 as pkd
+    pkd.load()   # the CUDA library must be built; there is no other path
+    ranks = Ranks()
+    try:
+        line = run_ours(args, ranks)
+        if ranks.rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        ranks.close()
+    return 0
+
+
+def _single_rank():
+    r = Ranks.__new__(Ranks)
+    r.world, r.rank, r.local, r.dist, r.backend = 1, 0, 0, None, "none"
+    return r
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,216 @@
+/*
+ * pkd.h - paged KV decode attention with split-KV partial states and the
+ * log-sum-exp merge, for NVIDIA GB300 (sm_103a).
+ *
+ * A C ABI: plain pointers and sizes, no C++ or framework types.  Every call
+ * returns a pkd_status; pkd_last_error() gives a message for the calling
+ * thread's last failure.  No call throws, aborts or allocates device memory:
+ * the caller owns every buffer (tensors, page tables, workspaces, pinned
+ * staging memory and the pkd_plan_t itself).
+ *
+ * Sources (page title, section):
+ *  [W] "FlashInfer" (aiwiki.ai/wiki/flashinfer)
+ *  [D] "Welcome to FlashInfer's documentation!" (docs.flashinfer.ai)
+ *
+ * Shapes and layouts (B requests, Hq query heads, Hkv key/value heads,
+ * g = Hq / Hkv, D = head_dim, P = page_size):
+ *  q          [B][Hq][D]                      dtype
+ *  k_pages    [num_pages][P][Hkv][D]          dtype  (NHD, [D] tutorial
+ *  v_pages    [num_pages][P][Hkv][D]          dtype   "KV-Cache Layout")
+ *  kv_indptr  [B + 1] int32, kv_indices [kv_indptr[B]] int32,
+ *  kv_last_page_len [B] int32: CSR page table ([D] "Page Table Layout";
+ *    [W] "Block-sparse cache representation").  Request b owns pages
+ *    kv_indices[kv_indptr[b] .. kv_indptr[b+1]) in sequence order; all are
+ *    full except the last, which holds kv_last_page_len[b] in [1, P] tokens.
+ *    A request with no pages is empty.  Page ids lie in [0, num_pages);
+ *    several requests may list the same page (shared prefixes).
+ *  out        [B][Hq][D] dtype;  lse [B][Hq] float (natural log).
+ *  Query head h attends with key/value head h / g ([W] "Custom attention
+ *  templates": grouped-query heads).
+ *
+ * Semantics: out[b,h] = sum_t softmax_t(s) v_t and lse[b,h] = log sum_t
+ * exp(s_t) with s_t = sm_scale * <q[b,h], k_t>, over the request's tokens.
+ * The running maximum starts at -infinity and an empty request yields
+ * out = 0, lse = -infinity ([W] "Extreme-negative-logit correction").
+ *
+ * Supported: dtype PKD_F16 or PKD_BF16; head_dim 128; Hkv in {1, 2, 4, 8};
+ * 1 <= g <= 16; page_size >= 1; 16-byte aligned device pointers.  Anything
+ * else returns PKD_ERR_UNSUPPORTED; there is no fallback path.
+ */
+#ifndef PKD_H
+#define PKD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKD_ABI_VERSION 1
+
+typedef enum {
+  PKD_OK = 0,
+  PKD_ERR_INVALID_ARG = -1,  /* null pointer, negative size, bad enum */
+  PKD_ERR_PAGE_TABLE = -2,   /* page table fails the CSR rules above */
+  PKD_ERR_WORKSPACE = -3,    /* a workspace or staging buffer is too small */
+  PKD_ERR_UNSUPPORTED = -4,  /* valid but outside the supported set */
+  PKD_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed */
+  PKD_ERR_DEVICE_CHECK = -6  /* a kernel recorded a failed check */
+} pkd_status;
+
+typedef enum { PKD_F16 = 0, PKD_BF16 = 1, PKD_F32 = 2 } pkd_dtype;
+
+/* Bits of the device status word (see pkd_check_status). */
+#define PKD_DEVICE_BAD_PAGE 1u    /* a page id outside [0, num_pages) */
+#define PKD_DEVICE_BAD_LENGTH 2u  /* a plan unit runs past the request */
+#define PKD_DEVICE_BAD_PLAN 4u    /* workspace does not hold a plan image */
+
+/* Problem geometry and planning knobs. */
+typedef struct {
+  int32_t batch;         /* B >= 0 */
+  int32_t num_qo_heads;  /* Hq */
+  int32_t num_kv_heads;  /* Hkv, Hq % Hkv == 0 */
+  int32_t head_dim;      /* D (128) */
+  int32_t page_size;     /* P >= 1 */
+  int32_t dtype;         /* pkd_dtype of q, k_pages, v_pages and out */
+  int64_t num_pages;     /* pages in the pool; bounds every page id */
+  int32_t num_ctas;      /* decode CTAs (one per SM is the intent); 0 = the
+                            current device's multiprocessor count */
+  int32_t min_chunks_per_request; /* each request of n tiles is cut into at
+                            least min(this, n) partial states; 0 or 1 = no
+                            minimum */
+  int32_t tile_tokens;   /* tokens per pipeline tile; 0 = 128 / Hkv (the
+                            decode kernel's tile); other values must equal it */
+  int32_t max_batch;     /* capacity used to size workspaces; 0 = batch */
+} pkd_problem;
+
+/* Result of planning: plain data, owned and stored by the caller. */
+typedef struct {
+  pkd_problem problem;          /* resolved copy (num_ctas, tile_tokens set) */
+  int32_t num_units;            /* work units in the plan */
+  int32_t num_partials;         /* partial-state slots used */
+  int32_t num_split_requests;   /* requests merged from >1 partial state */
+  int32_t total_tiles;          /* sum over requests of ceil(L_b / tile) */
+  int64_t total_tokens;         /* sum over requests of L_b */
+  int64_t int_ws_bytes_used;    /* bytes of the plan image */
+  int64_t float_ws_bytes_needed;/* bytes of partial states run() writes */
+  int32_t valid;                /* 1 once planned */
+  int32_t reserved;
+} pkd_plan_t;
+
+/* ABI version of the loaded library (PKD_ABI_VERSION). */
+int32_t pkd_abi_version(void);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char *pkd_last_error(void);
+
+/*
+ * Workspace sizes for a problem's capacity (max_batch, num_ctas,
+ * min_chunks_per_request), valid for every plan of that capacity:
+ *   int_ws_bytes   device buffer holding the plan image (int32 words);
+ *   float_ws_bytes device buffer for fp32 partial states;
+ *   staging_bytes  pinned host buffer pkd_plan() builds the image in.
+ * num_ctas == 0 queries the current device.  Any output pointer may be NULL.
+ */
+pkd_status pkd_workspace_size(const pkd_problem *problem,
+                              size_t *int_ws_bytes, size_t *float_ws_bytes,
+                              size_t *staging_bytes);
+
+/*
+ * Plans on the host only (no CUDA call): validates the page table, computes
+ * request lengths and the split-KV work list ([W] "Plan and run": planning
+ * reads sequence lengths and cache metadata, selects a schedule and prepares
+ * workspace data; "Attention states": a long cache is split across work units
+ * whose partial states are merged) and writes the plan image (int32 words)
+ * to host_image.  problem->num_ctas must be explicit (> 0).
+ * kv_indices_h may be NULL; if given, every page id is range-checked.
+ * Errors: PKD_ERR_INVALID_ARG, PKD_ERR_PAGE_TABLE, PKD_ERR_UNSUPPORTED,
+ * PKD_ERR_WORKSPACE (image larger than host_image_bytes).
+ */
+pkd_status pkd_plan_host(const pkd_problem *problem, const int32_t *kv_indptr_h,
+                         const int32_t *kv_last_page_len_h,
+                         const int32_t *kv_indices_h, pkd_plan_t *plan,
+                         int32_t *host_image, size_t host_image_bytes);
+
+/*
+ * pkd_plan_host into pinned_staging, then one asynchronous host-to-device
+ * copy of the image into int_ws_dev on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream).  The staging buffer must stay untouched until that
+ * copy has run.  Reusing int_ws_dev keeps device addresses stable across
+ * plans ([W] "Plan and run": stable workspace buffers, updated schedule data).
+ */
+pkd_status pkd_plan(const pkd_problem *problem, const int32_t *kv_indptr_h,
+                    const int32_t *kv_last_page_len_h,
+                    const int32_t *kv_indices_h, pkd_plan_t *plan,
+                    int32_t *pinned_staging, size_t staging_bytes,
+                    void *int_ws_dev, size_t int_ws_bytes, void *stream);
+
+/*
+ * Decode attention for a planned batch, on `stream`: the decode kernel walks
+ * the work list, writing out/lse directly for requests handled by one unit
+ * and fp32 partial (output, lse) states to float_ws_dev otherwise; then, if
+ * any request was split, the merge kernel combines each split request's
+ * partial states ([W] "Attention states").  Device pointers: q, k_pages,
+ * v_pages, the page table (the same table the plan saw), int_ws_dev (holding
+ * the plan image), float_ws_dev (>= plan->float_ws_bytes_needed), out, lse.
+ * Kernels range-check page ids and plan units against the device page table
+ * and record failures in the device status word instead of reading out of
+ * bounds.  Returns PKD_ERR_UNSUPPORTED / PKD_ERR_INVALID_ARG /
+ * PKD_ERR_WORKSPACE before launching, PKD_ERR_CUDA if a launch fails.
+ */
+pkd_status pkd_run(const pkd_plan_t *plan, const void *q, const void *k_pages,
+                   const void *v_pages, const int32_t *kv_indptr_d,
+                   const int32_t *kv_indices_d,
+                   const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                   void *float_ws_dev, size_t float_ws_bytes, float sm_scale,
+                   void *out, float *lse, void *stream);
+
+/*
+ * The two launches of pkd_run, for callers that put other work or events
+ * between them: pkd_run_decode launches the decode kernel (same arguments and
+ * errors as pkd_run); pkd_run_merge then launches the merge kernel for the
+ * plan's split requests, and does nothing when no request was split.  Both
+ * must see the same plan, workspaces and out/lse on streams ordered the same
+ * way as in pkd_run.
+ */
+pkd_status pkd_run_decode(const pkd_plan_t *plan, const void *q,
+                          const void *k_pages, const void *v_pages,
+                          const int32_t *kv_indptr_d, const int32_t *kv_indices_d,
+                          const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                          void *float_ws_dev, size_t float_ws_bytes,
+                          float sm_scale, void *out, float *lse, void *stream);
+
+pkd_status pkd_run_merge(const pkd_plan_t *plan, const void *int_ws_dev,
+                         const void *float_ws_dev, size_t float_ws_bytes,
+                         void *out, float *lse, void *stream);
+
+/*
+ * Merge of two attention states over disjoint regions into the state of
+ * their union ([W] "Attention states"; [D] flashinfer.cascade "Merge
+ * Attention States"): with M = max(s_a, s_b),
+ *   s = M + log(exp(s_a - M) + exp(s_b - M)),
+ *   v = exp(s_a - s) v_a + exp(s_b - s) v_b;
+ * a side with s = -infinity contributes nothing and two empty sides give
+ * (0, -infinity).  v_* are [n][num_heads][head_dim] of v_dtype (F16, BF16 or
+ * F32), s_* are [n][num_heads] float.  In-place use (v_out == v_a, s_out ==
+ * s_a) is allowed.  head_dim must be a multiple of 8 and at most 1024.
+ */
+pkd_status pkd_merge_states(const void *v_a, const float *s_a, const void *v_b,
+                            const float *s_b, void *v_out, float *s_out,
+                            int64_t n, int32_t num_heads, int32_t head_dim,
+                            int32_t v_dtype, void *stream);
+
+/*
+ * Reads the device status word of int_ws_dev (synchronising `stream`) into
+ * *device_status (PKD_DEVICE_* bits).  Returns PKD_ERR_DEVICE_CHECK if any
+ * bit is set, PKD_OK otherwise.  Planning clears the word.
+ */
+pkd_status pkd_check_status(const void *int_ws_dev, uint32_t *device_status,
+                            void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKD_H */

@@ -45,9 +45,19 @@ def compile_source(src: str, out: str) -> str:
     return out
 
 
+def _native(path: str) -> bool:
+    """True when the ELF file's machine field matches this host."""
+    import platform
+    want = {"x86_64": 62, "aarch64": 183}.get(platform.machine())
+    with open(path, "rb") as f:
+        head = f.read(20)
+    return want is None or (len(head) == 20 and
+                            int.from_bytes(head[18:20], "little") == want)
+
+
 def build(force: bool = False) -> str:
     """Compile ``ref_attn.c`` into ``libpkd_oracle.so`` (gcc, OpenMP)."""
-    if (not force and os.path.exists(_LIB)
+    if (not force and os.path.exists(_LIB) and _native(_LIB)
             and os.path.getmtime(_LIB) >= os.path.getmtime(SOURCE)):
         return _LIB
     return compile_source(SOURCE, _LIB)

@@ -1,0 +1,231 @@
+// C-ABI entry points declared in include/pkd.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <string>
+
+#include "pkd_internal.h"
+
+namespace {
+
+using pkd::fail;
+
+pkd_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(PKD_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Fills num_ctas from the current device when it is 0.
+pkd_status resolve_ctas(pkd_problem *p) {
+  if (p->num_ctas > 0) return PKD_OK;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "querying the multiprocessor count");
+  p->num_ctas = sms;
+  return PKD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pkd_abi_version(void) { return PKD_ABI_VERSION; }
+
+const char *pkd_last_error(void) { return pkd::last_error_cstr(); }
+
+pkd_status pkd_workspace_size(const pkd_problem *problem, size_t *int_ws_bytes,
+                              size_t *float_ws_bytes, size_t *staging_bytes) {
+  pkd::clear_error();
+  if (!problem) return fail(PKD_ERR_INVALID_ARG, "null problem");
+  pkd_problem p = *problem;
+  pkd_status st = resolve_ctas(&p);
+  if (st != PKD_OK) return st;
+  st = pkd::check_problem(p, true);
+  if (st != PKD_OK) return st;
+  pkd::workspace_bytes(p, int_ws_bytes, float_ws_bytes, staging_bytes);
+  return PKD_OK;
+}
+
+pkd_status pkd_plan_host(const pkd_problem *problem, const int32_t *kv_indptr_h,
+                         const int32_t *kv_last_page_len_h,
+                         const int32_t *kv_indices_h, pkd_plan_t *plan,
+                         int32_t *host_image, size_t host_image_bytes) {
+  pkd::clear_error();
+  if (!problem) return fail(PKD_ERR_INVALID_ARG, "null problem");
+  return pkd::plan_host_impl(*problem, kv_indptr_h, kv_last_page_len_h,
+                             kv_indices_h, plan, host_image, host_image_bytes);
+}
+
+pkd_status pkd_plan(const pkd_problem *problem, const int32_t *kv_indptr_h,
+                    const int32_t *kv_last_page_len_h,
+                    const int32_t *kv_indices_h, pkd_plan_t *plan,
+                    int32_t *pinned_staging, size_t staging_bytes,
+                    void *int_ws_dev, size_t int_ws_bytes, void *stream) {
+  pkd::clear_error();
+  if (!problem || !int_ws_dev) return fail(PKD_ERR_INVALID_ARG, "null pointer");
+  pkd_problem p = *problem;
+  pkd_status st = resolve_ctas(&p);
+  if (st != PKD_OK) return st;
+  st = pkd::plan_host_impl(p, kv_indptr_h, kv_last_page_len_h, kv_indices_h,
+                           plan, pinned_staging, staging_bytes);
+  if (st != PKD_OK) return st;
+  if (static_cast<size_t>(plan->int_ws_bytes_used) > int_ws_bytes) {
+    plan->valid = 0;
+    return fail(PKD_ERR_WORKSPACE, "int workspace smaller than the plan image");
+  }
+  cudaError_t e = cudaMemcpyAsync(int_ws_dev, pinned_staging,
+                                  static_cast<size_t>(plan->int_ws_bytes_used),
+                                  cudaMemcpyHostToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    plan->valid = 0;
+    return cuda_fail(e, "copying the plan image");
+  }
+  return PKD_OK;
+}
+
+pkd_status pkd_run_decode(const pkd_plan_t *plan, const void *q,
+                          const void *k_pages, const void *v_pages,
+                          const int32_t *kv_indptr_d, const int32_t *kv_indices_d,
+                          const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                          void *float_ws_dev, size_t float_ws_bytes,
+                          float sm_scale, void *out, float *lse, void *stream) {
+  pkd::clear_error();
+  if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "plan not valid");
+  const pkd_problem &p = plan->problem;
+  pkd_status st = pkd::check_problem(p, true);
+  if (st != PKD_OK) return st;
+  if (p.batch == 0) return PKD_OK;
+  if (!q || !out || !lse || !kv_indptr_d || !kv_last_page_len_d || !int_ws_dev)
+    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (plan->total_tokens > 0 && (!k_pages || !v_pages || !kv_indices_d))
+    return fail(PKD_ERR_INVALID_ARG, "null page pool or page ids");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      !aligned16(out) || !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
+    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
+  if (plan->num_partials > 0 &&
+      (!float_ws_dev ||
+       float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed)))
+    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the plan needs");
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f))
+    return fail(PKD_ERR_INVALID_ARG, "sm_scale must be finite and positive");
+
+  pkd::DecodeArgs a;
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.kv_indptr = kv_indptr_d;
+  a.kv_indices = kv_indices_d;
+  a.kv_last_page_len = kv_last_page_len_d;
+  a.image = static_cast<int32_t *>(int_ws_dev);
+  a.partials = static_cast<float *>(float_ws_dev);
+  a.out = out;
+  a.lse = lse;
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.num_pages = p.num_pages;
+  a.batch = p.batch;
+  a.num_qo_heads = p.num_qo_heads;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  a.num_ctas = p.num_ctas;
+  a.dtype = p.dtype;
+  a.max_partials = plan->num_partials;
+  a.image_words = static_cast<int>(plan->int_ws_bytes_used / 4);
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_decode(a, stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the decode kernel");
+  return PKD_OK;
+}
+
+pkd_status pkd_run_merge(const pkd_plan_t *plan, const void *int_ws_dev,
+                         const void *float_ws_dev, size_t float_ws_bytes,
+                         void *out, float *lse, void *stream) {
+  pkd::clear_error();
+  if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "plan not valid");
+  const pkd_problem &p = plan->problem;
+  pkd_status st = pkd::check_problem(p, true);
+  if (st != PKD_OK) return st;
+  if (plan->num_split_requests == 0) return PKD_OK;
+  if (!int_ws_dev || !float_ws_dev || !out || !lse)
+    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned16(out) || !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
+    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
+  if (float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed))
+    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the plan needs");
+  pkd::MergePartialsArgs m;
+  m.image = static_cast<const int32_t *>(int_ws_dev);
+  m.partials = static_cast<const float *>(float_ws_dev);
+  m.out = out;
+  m.lse = lse;
+  m.num_qo_heads = p.num_qo_heads;
+  m.dtype = p.dtype;
+  m.batch = p.batch;
+  m.max_partials = plan->num_partials;
+  m.image_words = static_cast<int>(plan->int_ws_bytes_used / 4);
+  const long long rows =
+      static_cast<long long>(plan->num_split_requests) * p.num_qo_heads;
+  const long long cap = 8LL * p.num_ctas;
+  m.grid = static_cast<int>(rows < cap ? rows : cap);
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_merge_partials(m, stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the merge kernel");
+  return PKD_OK;
+}
+
+pkd_status pkd_run(const pkd_plan_t *plan, const void *q, const void *k_pages,
+                   const void *v_pages, const int32_t *kv_indptr_d,
+                   const int32_t *kv_indices_d,
+                   const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                   void *float_ws_dev, size_t float_ws_bytes, float sm_scale,
+                   void *out, float *lse, void *stream) {
+  pkd_status st = pkd_run_decode(plan, q, k_pages, v_pages, kv_indptr_d,
+                                 kv_indices_d, kv_last_page_len_d, int_ws_dev,
+                                 float_ws_dev, float_ws_bytes, sm_scale, out, lse,
+                                 stream);
+  if (st != PKD_OK) return st;
+  return pkd_run_merge(plan, int_ws_dev, float_ws_dev, float_ws_bytes, out, lse,
+                       stream);
+}
+
+pkd_status pkd_merge_states(const void *v_a, const float *s_a, const void *v_b,
+                            const float *s_b, void *v_out, float *s_out,
+                            int64_t n, int32_t num_heads, int32_t head_dim,
+                            int32_t v_dtype, void *stream) {
+  pkd::clear_error();
+  if (n < 0 || num_heads <= 0 || head_dim <= 0)
+    return fail(PKD_ERR_INVALID_ARG, "negative or zero size");
+  if (v_dtype != PKD_F16 && v_dtype != PKD_BF16 && v_dtype != PKD_F32)
+    return fail(PKD_ERR_UNSUPPORTED, "v_dtype must be F16, BF16 or F32");
+  if (head_dim % 8 != 0 || head_dim > 1024)
+    return fail(PKD_ERR_UNSUPPORTED, "head_dim must be a multiple of 8, <= 1024");
+  if (n == 0) return PKD_OK;
+  if (!v_a || !s_a || !v_b || !s_b || !v_out || !s_out)
+    return fail(PKD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(v_a) || !aligned16(v_b) || !aligned16(v_out))
+    return fail(PKD_ERR_UNSUPPORTED, "state pointers must be 16-byte aligned");
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_merge_states(
+      v_a, s_a, v_b, s_b, v_out, s_out, n, num_heads, head_dim, v_dtype, stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching merge_states");
+  return PKD_OK;
+}
+
+pkd_status pkd_check_status(const void *int_ws_dev, uint32_t *device_status,
+                            void *stream) {
+  pkd::clear_error();
+  if (!int_ws_dev || !device_status) return fail(PKD_ERR_INVALID_ARG, "null pointer");
+  uint32_t word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(
+      &word, static_cast<const int32_t *>(int_ws_dev) + pkd::kHStatus,
+      sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  *device_status = word;
+  if (word != 0)
+    return fail(PKD_ERR_DEVICE_CHECK,
+                "device status word " + std::to_string(word));
+  return PKD_OK;
+}
+
+}  // extern "C"

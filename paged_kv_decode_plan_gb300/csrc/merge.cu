@@ -1,0 +1,234 @@
+// Attention-state merge kernels.
+//
+// "FlashInfer" (aiwiki.ai/wiki/flashinfer), "Attention states": states of
+// disjoint cache regions merge into the state of their union; the partial
+// outputs cannot be averaged, their log-sum-exp values give the rescaling to a
+// common normaliser.  With M the largest partial lse and w_i = exp(s_i - M):
+//   s = M + log(sum_i w_i),   v = sum_i w_i v_i / sum_i w_i.
+// A state with s = -infinity covers nothing and gets weight 0; if every state
+// is empty the result is (0, -infinity) ("Extreme-negative-logit
+// correction": no -inf - (-inf) reaches exp).
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "pkd_internal.h"
+#include "ptx.cuh"
+
+namespace pkd {
+namespace {
+
+constexpr int kMergeWarps = 8;
+constexpr int kMergeThreads = 32 * kMergeWarps;
+
+// Split-KV merge: one CTA per (split request, query head) row at a time; the
+// 8 warps take interleaved partial slots, lane l owns d = 4l .. 4l + 3.
+template <typename T>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_partials_kernel(const int32_t *image, const float *partials,
+                          uint16_t *out, float *lse, int hq, int batch,
+                          int max_partials, int image_words) {
+  __shared__ float4 red_acc[kMergeWarps][32];
+  __shared__ float red_w[kMergeWarps];
+  __shared__ float red_m[kMergeWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int num_ctas = image[kHNumCtas];
+  const int num_units = image[kHNumUnits];
+  const int num_split = image[kHNumSplit];
+  const int num_partials = image[kHNumPartials];
+  const ImageOffsets o = image_offsets(num_ctas, num_units, num_split);
+  // only an image the host planned for this launch is trusted (the decode
+  // kernel records a mismatch in the status word)
+  if (image[kHMagic] != kMagic || image[kHBatch] != batch ||
+      image[kHNumQoHeads] != hq || num_ctas < 0 || num_units < 0 ||
+      num_split < 0 || num_partials < 0 || num_partials > max_partials ||
+      o.end > image_words)
+    return;
+  const int32_t *merge_indptr = image + o.merge_indptr;
+  const int32_t *merge_req = image + o.merge_req;
+  const long long slot_floats = partial_slot_floats(hq, kHeadDim);
+  const long long rows = static_cast<long long>(num_split) * hq;
+
+  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int i = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
+    const int b = merge_req[i];
+    if (b < 0 || b >= batch) continue;
+    const int s0 = max(0, merge_indptr[i]);
+    const int s1 = min(num_partials, merge_indptr[i + 1]);
+
+    // pass 1: largest partial lse
+    float mx = -INFINITY;
+    for (int j = s0 + tid; j < s1; j += kMergeThreads)
+      mx = fmaxf(mx, partials[j * slot_floats + hq * kHeadDim + h]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red_m[warp] = mx;
+    __syncthreads();
+    mx = red_m[0];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) mx = fmaxf(mx, red_m[w]);
+    const float ref = mx == -INFINITY ? 0.f : mx;
+
+    // pass 2: weighted sum of the partial outputs
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+#pragma unroll 4
+    for (int j = s0 + warp; j < s1; j += kMergeWarps) {
+      const float *base = partials + j * slot_floats;
+      const float w = expf(base[hq * kHeadDim + h] - ref);
+      const float4 v = reinterpret_cast<const float4 *>(base + h * kHeadDim)[lane];
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+      wsum += w;
+    }
+    red_acc[warp][lane] = acc;
+    if (lane == 0) red_w[warp] = wsum;
+    __syncthreads();
+    if (warp == 0) {
+      float4 t = red_acc[0][lane];
+      float ws = red_w[0];
+#pragma unroll
+      for (int w = 1; w < kMergeWarps; ++w) {
+        const float4 r = red_acc[w][lane];
+        t.x += r.x;
+        t.y += r.y;
+        t.z += r.z;
+        t.w += r.w;
+        ws += red_w[w];
+      }
+      const float inv = ws > 0.f ? 1.f / ws : 0.f;
+      uint16_t *dst = out + (static_cast<long long>(b) * hq + h) * kHeadDim + 4 * lane;
+      uint2 packed;
+      packed.x = ptx::pack2<T>(t.x * inv, t.y * inv);
+      packed.y = ptx::pack2<T>(t.z * inv, t.w * inv);
+      *reinterpret_cast<uint2 *>(dst) = packed;
+      if (lane == 0)
+        lse[static_cast<long long>(b) * hq + h] = ws > 0.f ? ref + logf(ws) : -INFINITY;
+    }
+    __syncthreads();
+  }
+}
+
+// Pairwise merge of two states, one warp per (n, head) row; lane l handles
+// the 8-element chunks l, l + 32, ... of the row.
+template <typename V>
+struct Vec8;
+
+template <>
+struct Vec8<float> {
+  static __device__ __forceinline__ void load(const void *p, long long i, float (&x)[8]) {
+    const float4 *q = reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+    const float4 a = q[0], b = q[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+  static __device__ __forceinline__ void store(void *p, long long i, const float (&x)[8]) {
+    float4 *q = reinterpret_cast<float4 *>(static_cast<float *>(p) + i);
+    q[0] = make_float4(x[0], x[1], x[2], x[3]);
+    q[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+};
+
+template <typename T>
+struct Vec8Half {
+  static __device__ __forceinline__ void load(const void *p, long long i, float (&x)[8]) {
+    const uint4 r = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p) + i);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = ptx::unpack2<T>(w[k]);
+      x[2 * k] = f.x;
+      x[2 * k + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void store(void *p, long long i, const float (&x)[8]) {
+    uint4 r;
+    r.x = ptx::pack2<T>(x[0], x[1]);
+    r.y = ptx::pack2<T>(x[2], x[3]);
+    r.z = ptx::pack2<T>(x[4], x[5]);
+    r.w = ptx::pack2<T>(x[6], x[7]);
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p) + i) = r;
+  }
+};
+
+template <>
+struct Vec8<__half> : Vec8Half<__half> {};
+template <>
+struct Vec8<__nv_bfloat16> : Vec8Half<__nv_bfloat16> {};
+
+template <typename V>
+__global__ void __launch_bounds__(256)
+    merge_states_kernel(const void *v_a, const float *s_a, const void *v_b,
+                        const float *s_b, void *v_out, float *s_out,
+                        long long rows, int head_dim) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       row < rows; row += warps) {
+    const float sa = s_a[row], sb = s_b[row];
+    __syncwarp();  // every lane has read s before lane 0 may overwrite it
+    float wa = 0.f, wb = 0.f, inv = 0.f, s = -INFINITY;
+    if (!(sa == -INFINITY && sb == -INFINITY)) {
+      const float mx = fmaxf(sa, sb);
+      wa = expf(sa - mx);
+      wb = expf(sb - mx);
+      const float z = wa + wb;
+      inv = 1.f / z;
+      s = mx + logf(z);
+    }
+    for (int c = lane; c < head_dim / 8; c += 32) {
+      const long long i = row * head_dim + 8 * c;
+      float a[8], b[8], r[8];
+      Vec8<V>::load(v_a, i, a);
+      Vec8<V>::load(v_b, i, b);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) r[k] = (wa * a[k] + wb * b[k]) * inv;
+      Vec8<V>::store(v_out, i, r);
+    }
+    if (lane == 0) s_out[row] = s;
+  }
+}
+
+}  // namespace
+
+int launch_merge_partials(const MergePartialsArgs &a, void *stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a.dtype == PKD_BF16)
+    merge_partials_kernel<__nv_bfloat16><<<a.grid, kMergeThreads, 0, st>>>(
+        a.image, a.partials, static_cast<uint16_t *>(a.out), a.lse, a.num_qo_heads,
+        a.batch, a.max_partials, a.image_words);
+  else
+    merge_partials_kernel<__half><<<a.grid, kMergeThreads, 0, st>>>(
+        a.image, a.partials, static_cast<uint16_t *>(a.out), a.lse, a.num_qo_heads,
+        a.batch, a.max_partials, a.image_words);
+  return cudaGetLastError();
+}
+
+int launch_merge_states(const void *v_a, const float *s_a, const void *v_b,
+                        const float *s_b, void *v_out, float *s_out, int64_t n,
+                        int num_heads, int head_dim, int dtype, void *stream) {
+  const long long rows = static_cast<long long>(n) * num_heads;
+  if (rows == 0) return cudaSuccess;
+  const long long want = (rows + 7) / 8;
+  const int grid = static_cast<int>(want < 65535 * 16 ? want : 65535 * 16);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (dtype) {
+    case PKD_F32:
+      merge_states_kernel<float><<<grid, 256, 0, st>>>(v_a, s_a, v_b, s_b, v_out,
+                                                        s_out, rows, head_dim);
+      break;
+    case PKD_BF16:
+      merge_states_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+          v_a, s_a, v_b, s_b, v_out, s_out, rows, head_dim);
+      break;
+    default:
+      merge_states_kernel<__half><<<grid, 256, 0, st>>>(v_a, s_a, v_b, s_b, v_out,
+                                                         s_out, rows, head_dim);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkd

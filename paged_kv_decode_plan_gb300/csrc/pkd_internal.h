@@ -1,0 +1,112 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "pkd.h"
+
+#ifdef __CUDACC__
+#define PKD_HD __host__ __device__
+#else
+#define PKD_HD
+#endif
+
+namespace pkd {
+
+// Plan image layout (int32 words).  Header words:
+constexpr int kMagic = 0x31444B50;  // "PKD1"
+constexpr int kLayoutVersion = 1;
+constexpr int kHeaderWords = 16;
+enum HeaderWord {
+  kHMagic = 0,
+  kHVersion = 1,
+  kHBatch = 2,
+  kHNumCtas = 3,
+  kHNumUnits = 4,
+  kHNumPartials = 5,
+  kHNumSplit = 6,
+  kHTileTokens = 7,
+  kHPageSize = 8,
+  kHTotalTiles = 9,
+  kHQuota = 10,
+  kHMinChunks = 11,
+  kHStatus = 12,
+  kHNumQoHeads = 13,
+};
+constexpr int kUnitWords = 4;  // req, tok_begin, tok_end, partial slot (-1)
+
+// Word offsets of the arrays that follow the header.
+struct ImageOffsets {
+  int64_t cta_ptr, units, merge_indptr, merge_req, end;
+};
+PKD_HD inline ImageOffsets image_offsets(int64_t num_ctas, int64_t num_units,
+                                         int64_t num_split) {
+  ImageOffsets o;
+  o.cta_ptr = kHeaderWords;
+  o.units = o.cta_ptr + num_ctas + 1;
+  o.merge_indptr = o.units + kUnitWords * num_units;
+  o.merge_req = o.merge_indptr + num_split + 1;
+  o.end = o.merge_req + num_split;
+  return o;
+}
+
+// Partial states: per slot, o [Hq][D] floats then lse [Hq] floats padded to a
+// multiple of 4, so every o row starts 16-byte aligned.
+PKD_HD inline int64_t partial_slot_floats(int64_t hq, int64_t d) {
+  return hq * d + ((hq + 3) / 4) * 4;
+}
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxGroup = 16;
+inline int default_tile_tokens(int num_kv_heads) { return 128 / num_kv_heads; }
+
+// Thread-local error message; returns `status` for convenience.
+pkd_status fail(pkd_status status, const std::string &message);
+void clear_error();
+const char *last_error_cstr();
+
+// Validates the parts of a problem every entry point needs.
+pkd_status check_problem(const pkd_problem &p, bool need_ctas);
+int64_t max_units(const pkd_problem &p);
+
+// Workspace sizes for a problem with explicit num_ctas.
+void workspace_bytes(const pkd_problem &p, size_t *int_ws, size_t *float_ws,
+                     size_t *staging);
+
+// Planning on the host (plan.cpp).
+pkd_status plan_host_impl(const pkd_problem &in, const int32_t *kv_indptr,
+                          const int32_t *kv_last_page_len,
+                          const int32_t *kv_indices, pkd_plan_t *plan,
+                          int32_t *image, size_t image_bytes);
+
+// Launchers (decode.cu, merge.cu).  Return cudaError_t as int.
+struct DecodeArgs {
+  const void *q, *k_pages, *v_pages;
+  const int32_t *kv_indptr, *kv_indices, *kv_last_page_len;
+  int32_t *image;
+  float *partials;
+  void *out;
+  float *lse;
+  float sm_scale_log2;
+  int64_t num_pages;
+  int batch, num_qo_heads, num_kv_heads, page_size, num_ctas, dtype;
+  int max_partials, image_words;
+};
+int launch_decode(const DecodeArgs &a, void *stream);
+
+struct MergePartialsArgs {
+  const int32_t *image;
+  const float *partials;
+  void *out;
+  float *lse;
+  int num_qo_heads, dtype, grid, batch, max_partials, image_words;
+};
+int launch_merge_partials(const MergePartialsArgs &a, void *stream);
+
+int launch_merge_states(const void *v_a, const float *s_a, const void *v_b,
+                        const float *s_b, void *v_out, float *s_out, int64_t n,
+                        int num_heads, int head_dim, int dtype, void *stream);
+
+}  // namespace pkd

@@ -1,0 +1,90 @@
+"""GPU merge_states against the oracle merge ("FlashInfer"
+(aiwiki.ai/wiki/flashinfer), "Attention states"; -inf handling from
+"Extreme-negative-logit correction")."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_plan_gb300 as pkd
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def random_states(rng, n, h, d, dtype, empty_frac=0.2):
+    v = torch.from_numpy(rng.standard_normal((n, h, d)).astype(np.float32)).to(
+        DTYPES[dtype])
+    s = (rng.standard_normal((n, h)) * 20).astype(np.float32)
+    s[rng.random((n, h)) < empty_frac] = -np.inf
+    v_np = v.float().numpy()
+    v_np[np.isneginf(s)] = 0.0
+    v = torch.from_numpy(v_np).to(DTYPES[dtype])
+    return v, torch.from_numpy(s)
+
+
+def check(v, s, v_ref, s_ref, dtype):
+    v = v.float().cpu().numpy().reshape(v_ref.shape)
+    s = s.cpu().numpy().reshape(s_ref.shape)
+    both_empty = np.isneginf(s_ref)
+    assert np.all(np.isneginf(s[both_empty])) and np.all(v[both_empty] == 0)
+    tol = {"f32": 1e-5, "f16": 2e-3, "bf16": 1.6e-2}[dtype]
+    assert np.max(np.abs(v - v_ref)) <= tol
+    fin = ~both_empty
+    assert np.max(np.abs(s[fin] - s_ref[fin])) <= 1e-4 * np.maximum(1, np.abs(s_ref[fin])).max()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("n,h,d", [(1, 1, 8), (37, 32, 128), (128, 32, 128), (5, 3, 1024)])
+def test_merge_states_matches_oracle(dtype, n, h, d):
+    rng = np.random.default_rng(n * 1000 + h + d)
+    va, sa = random_states(rng, n, h, d, dtype)
+    vb, sb = random_states(rng, n, h, d, dtype)
+    out_v, out_s = pkd.merge_states(va.cuda(), sa.cuda(), vb.cuda(), sb.cuda())
+    torch.cuda.synchronize()
+    v_ref, s_ref = oracle.merge(va.double().numpy(), sa.double().numpy(),
+                                vb.double().numpy(), sb.double().numpy())
+    check(out_v, out_s, v_ref, s_ref, dtype)
+
+
+def test_merge_states_in_place_and_associative():
+    rng = np.random.default_rng(3)
+    n, h, d = 64, 8, 128
+    states = [random_states(rng, n, h, d, "f32", 0.1) for _ in range(3)]
+    dev = [(v.cuda(), s.cuda()) for v, s in states]
+    (va, sa), (vb, sb), (vc, sc) = dev
+    left = pkd.merge_states(*pkd.merge_states(va, sa, vb, sb), vc, sc)
+    bc = pkd.merge_states(vb, sb, vc, sc)
+    right = pkd.merge_states(va, sa, *bc)
+    torch.cuda.synchronize()
+    assert torch.allclose(left[0], right[0], atol=1e-5)
+    assert torch.allclose(left[1], right[1], atol=1e-4, equal_nan=False)
+    # in place: the output overwrites side a
+    va2, sa2 = va.clone(), sa.clone()
+    pkd.merge_states(va2, sa2, vb, sb, v_out=va2, s_out=sa2)
+    ref = pkd.merge_states(va, sa, vb, sb)
+    torch.cuda.synchronize()
+    assert torch.equal(va2, ref[0]) and torch.equal(sa2, ref[1])
+
+
+def test_merge_states_identity_and_both_empty():
+    n, h, d = 4, 2, 16
+    v = torch.randn(n, h, d, device="cuda", dtype=torch.float16)
+    s = torch.randn(n, h, device="cuda") * 5
+    empty_v = torch.zeros_like(v)
+    empty_s = torch.full_like(s, -float("inf"))
+    mv, ms = pkd.merge_states(v, s, empty_v, empty_s)
+    torch.cuda.synchronize()
+    assert torch.equal(mv, v) and torch.equal(ms, s)
+    mv, ms = pkd.merge_states(empty_v, empty_s, empty_v, empty_s)
+    torch.cuda.synchronize()
+    assert torch.all(mv == 0) and torch.all(torch.isneginf(ms))
+
+
+def test_merge_states_rejects_bad_shapes():
+    v = torch.zeros(2, 2, 12, device="cuda")
+    s = torch.zeros(2, 2, device="cuda")
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.merge_states(v, s, v, s)
+    assert e.value.status == -4
