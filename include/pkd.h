@@ -209,6 +209,35 @@ pkd_status pkd_merge_states(const void *v_a, const float *s_a, const void *v_b,
 pkd_status pkd_check_status(const void *int_ws_dev, uint32_t *device_status,
                             void *stream);
 
+/*
+ * pkd_run with no device allocation at all.  The pages have no counterpart to
+ * this call.  It is for callers that cannot allocate device memory when they
+ * decode: code whose device memory belongs to another allocator (a serving
+ * engine's pool, a plug-in inside a framework that forbids raw cudaMalloc) or
+ * a latency-critical loop that cannot pay for cudaMalloc / cudaFree, which may
+ * synchronise the device.  The plan image and the fp32 partial states live
+ * in a fixed __device__ array inside this library (256 KiB + 8 MiB, held by
+ * every GPU that loads the library until the process exits).
+ *
+ * plan and host_image come from pkd_plan_host; the image is copied into the
+ * array on `stream` (from pageable memory the call returns once the copy is
+ * staged; pinned memory must stay untouched until the stream passes the
+ * copy).  The other arguments are those of pkd_run.  A plan whose image
+ * exceeds 262144 bytes or whose partial states exceed 8388608 bytes returns
+ * PKD_ERR_WORKSPACE before any CUDA call; plan with a smaller
+ * min_chunks_per_request or split the batch.  The first call on a device
+ * looks up the array's address (with that device current); make it before
+ * any stream capture.  All calls share the array: calls that overlap on the
+ * GPU race.  Kernel range-check failures land in the array's copy of the
+ * status word and are not reported.
+ */
+pkd_status pkd_run_static(const pkd_plan_t *plan, const int32_t *host_image,
+                          const void *q, const void *k_pages,
+                          const void *v_pages, const int32_t *kv_indptr_d,
+                          const int32_t *kv_indices_d,
+                          const int32_t *kv_last_page_len_d, float sm_scale,
+                          void *out, float *lse, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

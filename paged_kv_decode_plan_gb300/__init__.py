@@ -30,7 +30,8 @@ STATUS_NAMES = {0: "PKD_OK", -1: "PKD_ERR_INVALID_ARG", -2: "PKD_ERR_PAGE_TABLE"
 # every symbol include/pkd.h declares
 EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
             "pkd_plan_host", "pkd_plan", "pkd_run", "pkd_run_decode",
-            "pkd_run_merge", "pkd_merge_states", "pkd_check_status")
+            "pkd_run_merge", "pkd_merge_states", "pkd_check_status",
+            "pkd_run_static")
 
 
 class PkdError(RuntimeError):
@@ -88,9 +89,11 @@ def load():
     lib.pkd_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int64,
                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp]
     lib.pkd_check_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.pkd_run_static.argtypes = [ctypes.POINTER(Plan), i32p, vp, vp, vp, vp, vp,
+                                   vp, ctypes.c_float, vp, vp, vp]
     for name in ("pkd_workspace_size", "pkd_plan_host", "pkd_plan", "pkd_run",
                  "pkd_run_decode", "pkd_run_merge", "pkd_merge_states",
-                 "pkd_check_status"):
+                 "pkd_check_status", "pkd_run_static"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.pkd_abi_version() != 1:
         raise RuntimeError("libpkd.so ABI version mismatch")
@@ -225,6 +228,28 @@ def run(plan_: Plan, q, k_pages, v_pages, kv_indptr, kv_indices, kv_last_page_le
               _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len),
               _ptr(int_ws), _ptr(float_ws), fbytes, float(sm_scale),
               _ptr(out), _ptr(lse), _stream_ptr(stream)))
+    return out, lse
+
+
+def run_static(plan_: Plan, host_image, q, k_pages, v_pages, kv_indptr, kv_indices,
+               kv_last_page_len, sm_scale: float, out=None, lse=None, stream=None):
+    """pkd_run_static: decode with the library's fixed device scratch array
+    instead of caller workspaces (for callers that cannot allocate device
+    memory).  ``plan_`` and ``host_image`` come from :func:`plan_host`."""
+    import torch
+    p = plan_.problem
+    if out is None:
+        out = torch.empty((p.batch, p.num_qo_heads, p.head_dim), dtype=q.dtype,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((p.batch, p.num_qo_heads), dtype=torch.float32,
+                          device=q.device)
+    image = np.ascontiguousarray(host_image, dtype=np.int32)
+    _check(load().pkd_run_static(
+        ctypes.byref(plan_), image.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_indptr), _ptr(kv_indices),
+        _ptr(kv_last_page_len), float(sm_scale), _ptr(out), _ptr(lse),
+        _stream_ptr(stream)))
     return out, lse
 
 
