@@ -65,6 +65,7 @@ typedef enum { PKD_F16 = 0, PKD_BF16 = 1, PKD_F32 = 2 } pkd_dtype;
 #define PKD_DEVICE_BAD_PAGE 1u    /* a page id outside [0, num_pages) */
 #define PKD_DEVICE_BAD_LENGTH 2u  /* a plan unit runs past the request */
 #define PKD_DEVICE_BAD_PLAN 4u    /* workspace does not hold a plan image */
+#define PKD_DEVICE_TIMEOUT 8u     /* a bounded pipeline wait ran out */
 
 /* Problem geometry and planning knobs. */
 typedef struct {
@@ -80,8 +81,8 @@ typedef struct {
   int32_t min_chunks_per_request; /* each request of n tiles is cut into at
                             least min(this, n) partial states; 0 or 1 = no
                             minimum */
-  int32_t tile_tokens;   /* tokens per pipeline tile; 0 = 128 / Hkv (the
-                            decode kernel's tile); other values must equal it */
+  int32_t tile_tokens;   /* tokens per pipeline tile; 0 = 16 (the decode
+                            kernel's tile); other values are unsupported */
   int32_t max_batch;     /* capacity used to size workspaces; 0 = batch */
 } pkd_problem;
 

@@ -22,7 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkd.so")
 
 PKD_F16, PKD_BF16, PKD_F32 = 0, 1, 2
-DEVICE_BAD_PAGE, DEVICE_BAD_LENGTH, DEVICE_BAD_PLAN = 1, 2, 4
+DEVICE_BAD_PAGE, DEVICE_BAD_LENGTH, DEVICE_BAD_PLAN, DEVICE_TIMEOUT = 1, 2, 4, 8
 STATUS_NAMES = {0: "PKD_OK", -1: "PKD_ERR_INVALID_ARG", -2: "PKD_ERR_PAGE_TABLE",
                 -3: "PKD_ERR_WORKSPACE", -4: "PKD_ERR_UNSUPPORTED",
                 -5: "PKD_ERR_CUDA", -6: "PKD_ERR_DEVICE_CHECK"}

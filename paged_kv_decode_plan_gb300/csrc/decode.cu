@@ -1,19 +1,31 @@
-// Split-KV paged decode attention kernel.
+// Split-KV paged decode attention kernel (warp-specialised).
 //
 // One persistent CTA per SM walks its contiguous share of the plan's work
-// list.  A unit is a token range [t0, t1) of one request; the CTA covers every
-// key/value head of that range, so each tile it loads is whole tokens (all
-// heads, NHD-contiguous in memory).  Tiles of 128 (token, head) rows of K and
-// V (64 KB) flow through a 3-stage cp.async pipeline into XOR-swizzled shared
-// memory; page ids are looked up one tile ahead of the copies that use them.
+// list.  A unit is a token range [t0, t1) of one request.  Tiles are 16
+// tokens of every key/value head (16 * Hkv * 512 bytes of K and V).
 //
-// Warp w handles key/value head w / (8 / Hkv) and 16 tokens of each tile.
-// The query group (g <= 16 heads) is the M = 16 side of mma.sync m16n8k16:
-//   S = Q K^T  (fp32 accumulate), online softmax in fp32 (base 2, with the
-//   scale sm_scale * log2(e) applied inside the exponent), O = O * alpha + P V.
-// P enters the second product in the input type (for bfloat16 as a hi + lo
-// pair); the row sums are taken over exactly the values multiplied, so O / l
-// stays a convex combination of the value rows.
+// Roles inside a CTA:
+//  * loader warp(s) fill a ring of shared-memory stages.  When a page holds
+//    whole 16-token tiles (page_size % 16 == 0) one warp issues TMA tiled
+//    loads (cp.async.bulk.tensor, 128-byte swizzle), one 16 x 64-element box
+//    per (tensor, head, d-half), completing on the stage's "full" mbarrier.
+//    Otherwise four warps copy 16-byte chunks with cp.async into the same
+//    swizzled layout and arrive on the barrier when their copies land.
+//  * eight consumer warps compute.  Warp w owns key/value head
+//    w / (8 / Hkv) and a slice of that head's query group, so no two warps
+//    share an output row.  With the query group as the N = 8 side of
+//    mma.sync m16n8k16:
+//        S^T = K Q^T    (16 tokens x 8 query heads, fp32 accumulate)
+//        online softmax over tokens in fp32, base 2, maxima kept on the raw
+//        logits and the scale sm_scale * log2(e) applied inside one fma;
+//        the reference is only moved when the maximum grows by more than
+//        2^8 (every p stays <= 256), so most tiles skip the rescale
+//        O^T += V^T P^T (128 d x 8 query heads); P^T reaches the B operand
+//        through movmatrix.  For bfloat16, P is split into hi + lo parts
+//        (8 significant bits each) and multiplied twice; row sums are taken
+//        over exactly the values multiplied.
+// Every mbarrier wait is bounded; a wait that runs out records
+// PKD_DEVICE_TIMEOUT in the status word and the CTA stops.
 //
 // Sources (page title, section):
 //  - "FlashInfer" (aiwiki.ai/wiki/flashinfer), "Block-sparse cache
@@ -24,9 +36,13 @@
 //  - same page, "Extreme-negative-logit correction": the running maximum
 //    starts at -infinity; differences are clamped so -inf - (-inf) never
 //    reaches exp; an empty row yields (0, -infinity).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstring>
+#include <mutex>
 #include <type_traits>
 
 #include "pkd_internal.h"
@@ -35,15 +51,26 @@
 namespace pkd {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = 3;
-constexpr int kRowBytes = kHeadDim * 2;                  // one token, one head
-constexpr int kTileRows = 128;                           // (token, head) rows
-constexpr int kTensorTileBytes = kTileRows * kRowBytes;  // 32 KB
-constexpr int kStageBytes = 2 * kTensorTileBytes;        // K then V
-constexpr int kRowsPerThread = kTileRows * 16 / kThreads;  // 16-byte chunks
+constexpr int kConsumerWarps = 8;
+constexpr int kTile = 16;                           // tokens per tile
+constexpr int kRowBytes = kHeadDim * 2;             // one token, one head
+constexpr int kHalfBytes = kTile * 128;             // 16 rows x 64 elements
+constexpr int kStageBudget = 3 * 64 * 1024;         // bytes of stages per CTA
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLazy = 8.f;                        // log2 of the largest p
+constexpr long long kWaitPolls = 1ll << 22;         // bounded mbarrier waits
+
+enum Loader : int { kLoaderTma = 0, kLoaderCpAsync = 1 };
+
+template <int L>
+__host__ __device__ constexpr int loader_warps() { return L == kLoaderTma ? 1 : 4; }
+__host__ __device__ constexpr int head_bytes() { return 2 * kHalfBytes; }  // one head
+template <int HKV>
+__host__ __device__ constexpr int tensor_bytes() { return HKV * head_bytes(); }
+template <int HKV>
+__host__ __device__ constexpr int stage_bytes() { return 2 * tensor_bytes<HKV>(); }
+template <int HKV>
+__host__ __device__ constexpr int num_stages() { return kStageBudget / stage_bytes<HKV>(); }
 
 struct Params {
   const uint16_t *q, *k, *v;
@@ -103,43 +130,110 @@ __device__ Unit read_unit(const Params &p, const int32_t *units, int u,
   return r;
 }
 
-// A tile ready to be copied: its first token, the unit's end, and the page id
-// and in-page slot of each of this thread's rows.
-struct TileDesc {
-  int tok0, t1;
-  int page[kRowsPerThread];
-  int slot[kRowsPerThread];
-};
+__device__ __forceinline__ int unit_tiles(const Unit &u) {
+  return (u.t1 - u.t0 + kTile - 1) / kTile;
+}
+
+// Polls an mbarrier phase; gives up (false) after kWaitPolls polls or once
+// another warp has given up.  `patient` waits ignore the abort flag.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           volatile int *abort, bool patient = false) {
+  for (long long i = 0; i < kWaitPolls; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (!patient && (i & 63) == 63 && *abort) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void give_up(const Params &p, volatile int *abort) {
+  *abort = 1;
+  flag(p.image, PKD_DEVICE_TIMEOUT);
+}
+
+// Byte offset of 16-byte chunk c (0..15) of token row r (0..15) within one
+// head's K or V tile: [d-half][row][128 B], chunks XOR-swizzled by row as the
+// TMA 128-byte swizzle lays them out.
+__device__ __forceinline__ uint32_t tile_offset(int r, int c) {
+  return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// ----------------------------------------------------------------- loaders
 
 template <int HKV>
-struct Pipeline {
-  static constexpr int kTile = kTileRows / HKV;  // tokens per tile
+__device__ void load_tma(const Params &p, const CUtensorMap *map_k,
+                         const CUtensorMap *map_v, const int32_t *units,
+                         int num_partials, int u_begin, int u_end, uint8_t *stages,
+                         uint32_t full0, uint32_t empty0, volatile int *abort) {
+  constexpr int kStages = num_stages<HKV>();
+  const int lane = threadIdx.x & 31;
+  const uint32_t stage0 = ptx::smem_u32(stages);
+  int it = 0;
+  bool ok = true;
+  for (int u = u_begin; u < u_end && ok; ++u) {
+    const Unit unit = read_unit(p, units, u, num_partials);
+    const int ntiles = unit_tiles(unit);
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = it % kStages;
+      if (!wait_phase(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, abort)) {
+        if (lane == 0) give_up(p, abort);
+        ok = false;
+        break;
+      }
+      const int tok0 = unit.t0 + t * kTile;
+      const int pi = tok0 / p.page_size;
+      const int slot0 = tok0 - pi * p.page_size;
+      int page = __ldg(p.indices + unit.pbase + pi);
+      if (static_cast<unsigned long long>(page) >=
+          static_cast<unsigned long long>(p.num_pages)) {
+        if (lane == 0) flag(p.image, PKD_DEVICE_BAD_PAGE);
+        page = 0;
+      }
+      if (lane == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes<HKV>());
+      __syncwarp();
+      if (lane < 4 * HKV) {
+        const int tensor = lane / (2 * HKV);
+        const int head = (lane >> 1) % HKV;
+        const int half = lane & 1;
+        const uint32_t dst = stage0 + s * stage_bytes<HKV>() +
+                             tensor * tensor_bytes<HKV>() + head * head_bytes() +
+                             half * kHalfBytes;
+        ptx::tma_load_3d(dst, tensor ? map_v : map_k, half * 64, head,
+                         page * p.page_size + slot0, full0 + 8 * s);
+      }
+      ++it;
+    }
+  }
+  // the CTA must not retire while this warp's copies are still landing
+  for (int j = max(0, it - kStages); j < it; ++j)
+    wait_phase(full0 + 8 * (j % kStages), (j / kStages) & 1, abort, true);
+}
+
+template <int HKV>
+struct CpAsyncLoader {
+  static constexpr int kRows = 2 * HKV;  // (token, head) rows per thread per tensor
 
   const Params &p;
   const int32_t *units;
-  int num_partials;
-  int u, u_end, t;  // cursor: next tile to describe is tile t of unit u
+  int num_partials, u, u_end, t;
   Unit unit;
-  bool have;        // desc holds a tile
-  TileDesc desc;
+  bool have;
+  int tok0, t1;
+  int page[kRows], slot[kRows];
 
-  __device__ Pipeline(const Params &p_, const int32_t *units_, int num_partials_,
-                      int u_begin, int u_end_)
-      : p(p_), units(units_), num_partials(num_partials_), u(u_begin),
-        u_end(u_end_), t(0), have(false) {
+  __device__ CpAsyncLoader(const Params &p_, const int32_t *units_, int np, int ub,
+                           int ue)
+      : p(p_), units(units_), num_partials(np), u(ub), u_end(ue), t(0), have(false) {
     if (u < u_end) unit = read_unit(p, units, u, num_partials);
     describe();
   }
 
-  // First token of this thread's row j within the tile, and its head.
-  __device__ __forceinline__ static int row_token(int j) {
-    return ((threadIdx.x >> 4) + 16 * j) / HKV;
+  __device__ __forceinline__ static int lt() {
+    return static_cast<int>(threadIdx.x) - 32 * kConsumerWarps;
   }
-  __device__ __forceinline__ static int row_head() {
-    return (threadIdx.x >> 4) % HKV;
-  }
+  __device__ __forceinline__ static int row_token(int j) { return ((lt() >> 4) + 8 * j) / HKV; }
+  __device__ __forceinline__ static int row_head(int j) { return ((lt() >> 4) + 8 * j) % HKV; }
 
-  // Advances the cursor to the next tile and loads its page ids.
+  // Moves to the next tile and starts the page-id loads it needs.
   __device__ void describe() {
     while (u < u_end && unit.t0 + t * kTile >= unit.t1) {
       ++u;
@@ -148,70 +242,302 @@ struct Pipeline {
     }
     have = u < u_end;
     if (!have) return;
-    desc.tok0 = unit.t0 + t * kTile;
-    desc.t1 = unit.t1;
+    tok0 = unit.t0 + t * kTile;
+    t1 = unit.t1;
 #pragma unroll
-    for (int j = 0; j < kRowsPerThread; ++j) {
-      const int tok = desc.tok0 + row_token(j);
-      int page = 0, slot = 0;
-      if (tok < desc.t1) {
+    for (int j = 0; j < kRows; ++j) {
+      const int tok = tok0 + row_token(j);
+      int pg = 0, sl = 0;
+      if (tok < t1) {
         const int pi = tok / p.page_size;
-        slot = tok - pi * p.page_size;
-        page = __ldg(p.indices + unit.pbase + pi);
+        sl = tok - pi * p.page_size;
+        pg = __ldg(p.indices + unit.pbase + pi);
       }
-      desc.page[j] = page;
-      desc.slot[j] = slot;
+      page[j] = pg;
+      slot[j] = sl;
     }
     ++t;
   }
 
-  // Copies the described tile into `stage` (zero rows past the unit's end),
-  // then describes the next one.  Always commits one cp.async group.
-  __device__ void issue(uint8_t *stage) {
-    if (have) {
-      const int c = threadIdx.x & 15;
-      const int head = row_head();
-      const uint32_t k_dst = ptx::smem_u32(stage);
-      const uint32_t v_dst = k_dst + kTensorTileBytes;
+  // Copies the described tile into the stage at `dst` (zero rows past the
+  // unit's end).
+  __device__ void issue(uint32_t dst) {
+    const int c = lt() & 15;
 #pragma unroll
-      for (int j = 0; j < kRowsPerThread; ++j) {
-        const int tl = row_token(j);
-        const int tok = desc.tok0 + tl;
-        bool valid = tok < desc.t1;
-        const int page = desc.page[j];
-        if (valid && static_cast<unsigned long long>(page) >=
-                         static_cast<unsigned long long>(p.num_pages)) {
-          flag(p.image, PKD_DEVICE_BAD_PAGE);
-          valid = false;
-        }
-        const long long row =
-            valid ? ((static_cast<long long>(page) * p.page_size + desc.slot[j]) *
-                         HKV + head)
-                  : 0;
-        const uint32_t off =
-            (head * kTile + tl) * kRowBytes + ((c ^ (tl & 7)) << 4);
-        const uint32_t n = valid ? 16u : 0u;
-        ptx::cp_async_16(k_dst + off, p.k + row * kHeadDim + c * 8, n);
-        ptx::cp_async_16(v_dst + off, p.v + row * kHeadDim + c * 8, n);
+    for (int j = 0; j < kRows; ++j) {
+      const int tl = row_token(j);
+      const int head = row_head(j);
+      bool valid = tok0 + tl < t1;
+      if (valid && static_cast<unsigned long long>(page[j]) >=
+                       static_cast<unsigned long long>(p.num_pages)) {
+        flag(p.image, PKD_DEVICE_BAD_PAGE);
+        valid = false;
       }
-      describe();
+      const long long row =
+          valid ? (static_cast<long long>(page[j]) * p.page_size + slot[j]) * HKV + head
+                : 0;
+      const uint32_t off = head * head_bytes() + tile_offset(tl, c);
+      const uint32_t n = valid ? 16u : 0u;
+      ptx::cp_async_16(dst + off, p.k + row * kHeadDim + c * 8, n);
+      ptx::cp_async_16(dst + tensor_bytes<HKV>() + off, p.v + row * kHeadDim + c * 8, n);
     }
-    ptx::cp_async_commit();
   }
 };
 
-template <typename T, int HKV>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p) {
-  constexpr int kWph = kWarps / HKV;  // warps per key/value head
-  constexpr int kTile = kTileRows / HKV;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  float *red_m = reinterpret_cast<float *>(smem + kStages * kStageBytes);
-  float *red_l = red_m + kWarps * 16;
-  float *red_acc = red_l + HKV * 16;
+template <int HKV>
+__device__ void load_cp_async(const Params &p, const int32_t *units, int num_partials,
+                              int u_begin, int u_end, uint8_t *stages, uint32_t full0,
+                              uint32_t empty0, volatile int *abort) {
+  constexpr int kStages = num_stages<HKV>();
+  const uint32_t stage0 = ptx::smem_u32(stages);
+  CpAsyncLoader<HKV> ld(p, units, num_partials, u_begin, u_end);
+  int it = 0;
+  while (ld.have) {
+    const int s = it % kStages;
+    if (!wait_phase(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, abort)) {
+      give_up(p, abort);
+      break;
+    }
+    ld.issue(stage0 + s * stage_bytes<HKV>());
+    ptx::cp_async_mbar_arrive_noinc(full0 + 8 * s);
+    ld.describe();
+    ++it;
+  }
+  ptx::cp_async_wait_all();
+}
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hk = warp / kWph, sub = warp % kWph;
+// ---------------------------------------------------------------- consumer
+
+template <typename T, int HKV, int NG>
+__device__ void consume(const Params &p, const int32_t *units, int num_partials,
+                        int u_begin, int u_end, const uint8_t *stages, uint32_t full0,
+                        uint32_t empty0, volatile int *abort) {
+  constexpr int kStages = num_stages<HKV>();
+  constexpr int kQw = kConsumerWarps / HKV;       // warps per key/value head
+  constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hk = warp / kQw, qpart = warp % kQw;
   const int gid = lane >> 2, tq = lane & 3;
+  const int gq = (p.group + kQw - 1) / kQw;       // query heads per warp
+  const int col_lo = qpart * gq;
+  const int col_hi = min(p.group, col_lo + gq);   // this warp's columns
+  const float c = p.scale_log2;
+  const uint32_t stage0 = ptx::smem_u32(stages);
+  const int slot_floats = static_cast<int>(partial_slot_floats(p.hq, kHeadDim));
+  // ldmatrix row addresses: K as the A operand (non-transposed), V^T as the
+  // A operand (transposed load of V rows)
+  const int a_row = (lane & 7) + (((lane >> 3) & 1) << 3);
+  const int a_hi = lane >> 4;
+  const int v_row = (lane & 7) + ((lane >> 4) << 3);
+  const int v_hi = (lane >> 3) & 1;
+
+  int it = 0;
+  for (int u = u_begin; u < u_end; ++u) {
+    const Unit unit = read_unit(p, units, u, num_partials);
+    const int ntiles = unit_tiles(unit);
+
+    // Q^T as the B operand: column n*8 + gid is query head col_lo + n*8 + gid
+    uint32_t qb[NG][8][2];
+#pragma unroll
+    for (int n = 0; n < NG; ++n) {
+      const int col = col_lo + 8 * n + gid;
+      const bool ok = unit.req >= 0 && col < col_hi;
+      const uint16_t *qrow =
+          p.q + (static_cast<long long>(max(unit.req, 0)) * p.hq + hk * p.group +
+                 min(col, p.group - 1)) * kHeadDim;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qb[n][kk][0] =
+            ok ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tq)) : 0u;
+        qb[n][kk][1] =
+            ok ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 8 + 2 * tq)) : 0u;
+      }
+    }
+
+    float ref[NG][2], l[NG][2], acc[NG][8][4];
+#pragma unroll
+    for (int n = 0; n < NG; ++n) {
+      ref[n][0] = ref[n][1] = -INFINITY;
+      l[n][0] = l[n][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+        acc[n][mt][0] = acc[n][mt][1] = acc[n][mt][2] = acc[n][mt][3] = 0.f;
+    }
+
+    bool stop = false;
+    for (int t = 0; t < ntiles; ++t, ++it) {
+      const int s = it % kStages;
+      if (!wait_phase(full0 + 8 * s, (it / kStages) & 1, abort)) {
+        if (lane == 0) give_up(p, abort);
+        stop = true;
+        break;
+      }
+      const uint32_t kb = stage0 + s * stage_bytes<HKV>() + hk * head_bytes();
+      const uint32_t vb = kb + tensor_bytes<HKV>();
+      const int valid = min(kTile, unit.t1 - unit.t0 - t * kTile);
+
+      // S^T = K Q^T: rows are tokens, columns this warp's query heads
+      float sc[NG][4];
+#pragma unroll
+      for (int n = 0; n < NG; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a[4];
+        ptx::ldmatrix_x4(kb + tile_offset(a_row, 2 * kk + a_hi), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int n = 0; n < NG; ++n) ptx::mma_16816<T>(sc[n], a, qb[n][kk][0], qb[n][kk][1]);
+      }
+
+      // online softmax over tokens, per query-head column
+      bool need = false;
+      float cand[NG][2];
+#pragma unroll
+      for (int n = 0; n < NG; ++n) {
+        if (gid >= valid) sc[n][0] = sc[n][1] = -INFINITY;
+        if (gid + 8 >= valid) sc[n][2] = sc[n][3] = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float mx = fmaxf(sc[n][j], sc[n][j + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          cand[n][j] = mx * c;
+          need |= cand[n][j] > ref[n][j] + kLazy;
+        }
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int n = 0; n < NG; ++n)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float alpha = 1.f;
+            if (cand[n][j] > ref[n][j] + kLazy) {
+              alpha = exp2f(ref[n][j] - cand[n][j]);  // ref = -inf gives 0
+              ref[n][j] = cand[n][j];
+            }
+            l[n][j] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              acc[n][mt][j] *= alpha;
+              acc[n][mt][j + 2] *= alpha;
+            }
+          }
+      }
+
+      // P^T as the B operand of O^T += V^T P^T
+      uint32_t pb[NG][2], pl[NG][2];
+#pragma unroll
+      for (int n = 0; n < NG; ++n) {
+        const float r0 = ref[n][0] == -INFINITY ? 0.f : ref[n][0];  // clamp
+        const float r1 = ref[n][1] == -INFINITY ? 0.f : ref[n][1];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float e0 = exp2f(fmaf(sc[n][2 * h], c, -r0));
+          const float e1 = exp2f(fmaf(sc[n][2 * h + 1], c, -r1));
+          const uint32_t hi = ptx::pack2<T>(e0, e1);
+          const float2 bh = ptx::unpack2<T>(hi);
+          pb[n][h] = ptx::movmatrix_trans(hi);
+          if (kSplitP) {
+            const uint32_t lo = ptx::pack2<T>(e0 - bh.x, e1 - bh.y);
+            const float2 bl = ptx::unpack2<T>(lo);
+            pl[n][h] = ptx::movmatrix_trans(lo);
+            l[n][0] += bh.x + bl.x;
+            l[n][1] += bh.y + bl.y;
+          } else {
+            pl[n][h] = 0u;
+            l[n][0] += bh.x;
+            l[n][1] += bh.y;
+          }
+        }
+      }
+
+      // V rows past the unit's end may hold anything: zero them in the A
+      // fragments (tokens 2tq, 2tq+1 and 2tq+8, 2tq+9 of this lane)
+      uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
+      if (valid < kTile) {
+        m01 = (2 * tq < valid ? 0x0000ffffu : 0u) | (2 * tq + 1 < valid ? 0xffff0000u : 0u);
+        m89 = (2 * tq + 8 < valid ? 0x0000ffffu : 0u) |
+              (2 * tq + 9 < valid ? 0xffff0000u : 0u);
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a[4];
+        ptx::ldmatrix_x4_trans(vb + tile_offset(v_row, 2 * mt + v_hi), a[0], a[1], a[2],
+                               a[3]);
+        a[0] &= m01;
+        a[1] &= m01;
+        a[2] &= m89;
+        a[3] &= m89;
+#pragma unroll
+        for (int n = 0; n < NG; ++n) {
+          ptx::mma_16816<T>(acc[n][mt], a, pb[n][0], pb[n][1]);
+          if (kSplitP) ptx::mma_16816<T>(acc[n][mt], a, pl[n][0], pl[n][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(empty0 + 8 * s);
+    }
+    if (stop) return;
+
+    // column sums across the eight token rows of the fragment
+#pragma unroll
+    for (int n = 0; n < NG; ++n)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        l[n][j] += __shfl_xor_sync(0xffffffffu, l[n][j], 4);
+        l[n][j] += __shfl_xor_sync(0xffffffffu, l[n][j], 8);
+        l[n][j] += __shfl_xor_sync(0xffffffffu, l[n][j], 16);
+      }
+    if (unit.req < 0) continue;
+#pragma unroll
+    for (int n = 0; n < NG; ++n)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = col_lo + 8 * n + 2 * tq + j;
+        if (col >= col_hi) continue;
+        const int head = hk * p.group + col;
+        const float inv = l[n][j] > 0.f ? 1.f / l[n][j] : 0.f;
+        const float lse_h =
+            l[n][j] > 0.f ? (ref[n][j] + log2f(l[n][j])) * kLn2 : -INFINITY;
+        if (unit.slot < 0) {
+          uint16_t *o = p.out + (static_cast<long long>(unit.req) * p.hq + head) * kHeadDim;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const uint32_t pair =
+                ptx::pack2<T>(acc[n][mt][j] * inv, acc[n][mt][j + 2] * inv);
+            o[16 * mt + gid] = static_cast<uint16_t>(pair & 0xffffu);
+            o[16 * mt + gid + 8] = static_cast<uint16_t>(pair >> 16);
+          }
+          if (gid == 0) p.lse[static_cast<long long>(unit.req) * p.hq + head] = lse_h;
+        } else {
+          float *base = p.partials + static_cast<long long>(unit.slot) * slot_floats;
+          float *o = base + head * kHeadDim;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[16 * mt + gid] = acc[n][mt][j] * inv;
+            o[16 * mt + gid + 8] = acc[n][mt][j + 2] * inv;
+          }
+          if (gid == 0) base[p.hq * kHeadDim + head] = lse_h;
+        }
+      }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <typename T, int HKV, int NG, int LOADER>
+__global__ void __launch_bounds__(32 * (kConsumerWarps + loader_warps<LOADER>()), 1)
+    decode_kernel(const __grid_constant__ Params p,
+                  const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v) {
+  constexpr int kStages = num_stages<HKV>();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *stages = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(stages + kStages * stage_bytes<HKV>());
+  volatile int *abort = reinterpret_cast<volatile int *>(bars + 2 * kStages);
+  const uint32_t full0 = ptx::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kStages;
 
   // the image must be the one the host planned for this launch
   const int32_t *img = p.image;
@@ -224,271 +550,119 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p) {
       num_ctas != p.grid || num_units < 0 || num_partials < 0 ||
       num_partials > p.max_partials || img[kHNumSplit] < 0 ||
       image_offsets(num_ctas, num_units, img[kHNumSplit]).end > p.image_words) {
-    if (tid == 0 && blockIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
+    if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
     return;
   }
   const int32_t *cta_ptr = img + kHeaderWords;
   const int32_t *units = cta_ptr + num_ctas + 1;
   const int u_begin = cta_ptr[blockIdx.x], u_end = cta_ptr[blockIdx.x + 1];
   if (u_begin < 0 || u_end > num_units || u_begin > u_end) {
-    if (tid == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
+    if (threadIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
     return;
   }
   if (u_begin == u_end) return;
 
-  if (kWph > 1) {
-    for (int i = tid; i < HKV * 16 * (kHeadDim + 1); i += kThreads) red_l[i] = 0.f;
+  if (threadIdx.x == 0) {
+    const uint32_t full_count =
+        LOADER == kLoaderTma ? 1u : 32u * loader_warps<kLoaderCpAsync>();
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full0 + 8 * s, full_count);
+      ptx::mbar_init(empty0 + 8 * s, kConsumerWarps);
+    }
+    *abort = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async();
   }
+  __syncthreads();
 
-  Pipeline<HKV> pipe(p, units, num_partials, u_begin, u_end);
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) pipe.issue(smem + s * kStageBytes);
-
-  // per-lane ldmatrix addressing (token within the warp's 16, swizzle key)
-  const int k_tok = (lane & 7) + ((lane >> 4) << 3);
-  const int k_hi = (lane >> 3) & 1;
-  const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-  const int v_hi = lane >> 4;
-  const int sw = lane & 7;
-  const int slot_floats = static_cast<int>(partial_slot_floats(p.hq, kHeadDim));
-
-  int stage = 0;
-  for (int u = u_begin; u < u_end; ++u) {
-    const Unit unit = read_unit(p, units, u, num_partials);
-
-    // query fragments: rows are the group's heads (zero past g)
-    uint32_t qf[8][4];
-    {
-      const int r0 = gid, r1 = gid + 8;
-      const uint16_t *q0 = p.q + (static_cast<long long>(max(unit.req, 0)) * p.hq +
-                                  hk * p.group + r0) * kHeadDim;
-      const uint16_t *q1 = q0 + 8 * kHeadDim;
-      const bool ok0 = unit.req >= 0 && r0 < p.group;
-      const bool ok1 = unit.req >= 0 && r1 < p.group;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int d = kk * 16 + 2 * tq;
-        qf[kk][0] = ok0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + d)) : 0u;
-        qf[kk][1] = ok1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + d)) : 0u;
-        qf[kk][2] = ok0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + d + 8)) : 0u;
-        qf[kk][3] = ok1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + d + 8)) : 0u;
-      }
-    }
-
-    float m[2] = {-INFINITY, -INFINITY};  // running max of the raw logits
-    float l[2] = {0.f, 0.f};              // this lane's share of the row sums
-    float acc[16][4];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-    const int ntiles = (unit.t1 - unit.t0 + kTile - 1) / kTile;
-    for (int it = 0; it < ntiles; ++it) {
-      ptx::cp_async_wait<kStages - 2>();
-      __syncthreads();
-      pipe.issue(smem + ((stage + kStages - 1) % kStages) * kStageBytes);
-
-      const uint8_t *sk = smem + stage * kStageBytes;
-      const uint32_t kbase =
-          ptx::smem_u32(sk) + (hk * kTile + sub * 16) * kRowBytes;
-      const uint32_t vbase = kbase + kTensorTileBytes;
-      const int valid = min(kTile, unit.t1 - unit.t0 - it * kTile) - sub * 16;
-
-      // S = Q K^T over this warp's 16 tokens
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t b0, b1, b2, b3;
-        ptx::ldmatrix_x4(kbase + k_tok * kRowBytes + (((2 * kk + k_hi) ^ sw) << 4),
-                         b0, b1, b2, b3);
-        ptx::mma_16816<T>(s[0], qf[kk], b0, b1);
-        ptx::mma_16816<T>(s[1], qf[kk], b2, b3);
-      }
-
-      // online softmax (rows gid and gid + 8).  Maxima are kept on the raw
-      // logits; the scaled difference s * c - m * c is formed inside one fma so
-      // only that small difference is rounded, and a row whose maximum is
-      // still -inf uses reference 0 (clamp: no -inf - (-inf)).
-      float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tok = n * 8 + 2 * tq + (i & 1);
-          if (tok >= valid) s[n][i] = -INFINITY;
-          mx[i >> 1] = fmaxf(mx[i >> 1], s[n][i]);
-        }
-      float ref[2], alpha[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        const float mn = fmaxf(m[r], mx[r]);
-        ref[r] = mn == -INFINITY ? 0.f : mn * p.scale_log2;
-        alpha[r] = exp2f(fmaf(m[r], p.scale_log2, -ref[r]));
-        m[r] = mn;
-      }
-      // P as the A operand of P V.  bfloat16 keeps only 8 significant bits,
-      // so for it P is split into hi + lo (both bf16) and multiplied twice;
-      // half P is used once.  Row sums are taken over the values multiplied.
-      constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
-      uint32_t pa[4], pb[4];
-      float rs[2] = {0.f, 0.f};
-#pragma unroll
-      for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float e0 = exp2f(fmaf(s[n][2 * h], p.scale_log2, -ref[h]));
-          const float e1 = exp2f(fmaf(s[n][2 * h + 1], p.scale_log2, -ref[h]));
-          const uint32_t hi = ptx::pack2<T>(e0, e1);
-          const float2 back = ptx::unpack2<T>(hi);
-          pa[2 * n + h] = hi;
-          if (kSplitP) {
-            const uint32_t lo = ptx::pack2<T>(e0 - back.x, e1 - back.y);
-            const float2 back_lo = ptx::unpack2<T>(lo);
-            pb[2 * n + h] = lo;
-            rs[h] += (back.x + back_lo.x) + (back.y + back_lo.y);
-          } else {
-            pb[2 * n + h] = 0u;
-            rs[h] += back.x + back.y;
-          }
-        }
-#pragma unroll
-      for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + rs[r];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        acc[j][0] *= alpha[0];
-        acc[j][1] *= alpha[0];
-        acc[j][2] *= alpha[1];
-        acc[j][3] *= alpha[1];
-      }
-
-      // O += P V
-#pragma unroll
-      for (int jj = 0; jj < 16; jj += 2) {
-        uint32_t b0, b1, b2, b3;
-        ptx::ldmatrix_x4_trans(
-            vbase + v_tok * kRowBytes + (((jj + v_hi) ^ sw) << 4), b0, b1, b2, b3);
-        ptx::mma_16816<T>(acc[jj], pa, b0, b1);
-        ptx::mma_16816<T>(acc[jj + 1], pa, b2, b3);
-        if (kSplitP) {
-          ptx::mma_16816<T>(acc[jj], pb, b0, b1);
-          ptx::mma_16816<T>(acc[jj + 1], pb, b2, b3);
-        }
-      }
-      stage = (stage + 1) % kStages;
-    }
-
-    // row totals of l across the quad
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-      l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-    }
-
-    bool writer = true;
-    if (kWph > 1) {
-      // combine the warps that share this head: rescale to the common max
-      if (tq == 0) {
-        red_m[warp * 16 + gid] = m[0];
-        red_m[warp * 16 + gid + 8] = m[1];
-      }
-      __syncthreads();
-      float f[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float mm = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWph; ++w)
-          mm = fmaxf(mm, red_m[(hk * kWph + w) * 16 + gid + 8 * r]);
-        const float rf = mm == -INFINITY ? 0.f : mm * p.scale_log2;
-        f[r] = exp2f(fmaf(m[r], p.scale_log2, -rf));
-        m[r] = mm;
-      }
-      float *acc_h = red_acc + hk * 16 * kHeadDim;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          atomicAdd(acc_h + (gid + 8 * (i >> 1)) * kHeadDim + 8 * j + 2 * tq + (i & 1),
-                    acc[j][i] * f[i >> 1]);
-      if (tq == 0) {
-        atomicAdd(red_l + hk * 16 + gid, l[0] * f[0]);
-        atomicAdd(red_l + hk * 16 + gid + 8, l[1] * f[1]);
-      }
-      __syncthreads();
-      writer = sub == 0;
-      if (writer) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float *cell =
-                acc_h + (gid + 8 * (i >> 1)) * kHeadDim + 8 * j + 2 * tq + (i & 1);
-            acc[j][i] = *cell;
-            *cell = 0.f;
-          }
-        l[0] = red_l[hk * 16 + gid];
-        l[1] = red_l[hk * 16 + gid + 8];
-      }
-      __syncthreads();
-      if (writer && tq == 0) {
-        red_l[hk * 16 + gid] = 0.f;
-        red_l[hk * 16 + gid + 8] = 0.f;
-      }
-    }
-
-    if (writer && unit.req >= 0) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int row = gid + 8 * r;
-        if (row >= p.group) continue;
-        const int head = hk * p.group + row;
-        const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
-        const float lse_r =
-            l[r] > 0.f ? fmaf(m[r], p.scale_log2, log2f(l[r])) * kLn2 : -INFINITY;
-        if (unit.slot < 0) {
-          uint16_t *o = p.out + (static_cast<long long>(unit.req) * p.hq + head) * kHeadDim;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<uint32_t *>(o + 8 * j + 2 * tq) =
-                ptx::pack2<T>(acc[j][2 * r] * inv, acc[j][2 * r + 1] * inv);
-          if (tq == 0) p.lse[static_cast<long long>(unit.req) * p.hq + head] = lse_r;
-        } else {
-          float *base = p.partials + static_cast<long long>(unit.slot) * slot_floats;
-          float *o = base + head * kHeadDim;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<float2 *>(o + 8 * j + 2 * tq) =
-                make_float2(acc[j][2 * r] * inv, acc[j][2 * r + 1] * inv);
-          if (tq == 0) base[p.hq * kHeadDim + head] = lse_r;
-        }
-      }
-    }
+  if (threadIdx.x >= 32 * kConsumerWarps) {
+    if (LOADER == kLoaderTma)
+      load_tma<HKV>(p, &map_k, &map_v, units, num_partials, u_begin, u_end, stages,
+                    full0, empty0, abort);
+    else
+      load_cp_async<HKV>(p, units, num_partials, u_begin, u_end, stages, full0,
+                         empty0, abort);
+  } else {
+    consume<T, HKV, NG>(p, units, num_partials, u_begin, u_end, stages, full0,
+                        empty0, abort);
   }
-  ptx::cp_async_wait<0>();
 }
 
-template <typename T, int HKV>
-int launch_typed(const Params &prm, int grid, void *stream) {
-  constexpr int kWph = kWarps / HKV;
-  const int smem = kStages * kStageBytes +
-                   (kWph > 1 ? (kWarps * 16 + HKV * 16 * (1 + kHeadDim)) * 4 : 0);
-  auto kernel = decode_kernel<T, HKV>;
-  cudaError_t e = cudaFuncSetAttribute(
-      kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <int HKV>
+__host__ __device__ constexpr int smem_bytes() {
+  return 1024 + num_stages<HKV>() * stage_bytes<HKV>() + 16 * num_stages<HKV>() + 16;
+}
+
+template <typename T, int HKV, int NG, int LOADER>
+int launch_typed(const Params &prm, const CUtensorMap &mk, const CUtensorMap &mv,
+                 void *stream) {
+  auto kernel = decode_kernel<T, HKV, NG, LOADER>;
+  const int smem = smem_bytes<HKV>();
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(prm);
+  kernel<<<prm.grid, 32 * (kConsumerWarps + loader_warps<LOADER>()), smem,
+           static_cast<cudaStream_t>(stream)>>>(prm, mk, mv);
   return cudaGetLastError();
 }
 
+template <typename T, int HKV, int NG>
+int launch_loader(const Params &prm, bool tma, const CUtensorMap &mk,
+                  const CUtensorMap &mv, void *stream) {
+  if (tma) return launch_typed<T, HKV, NG, kLoaderTma>(prm, mk, mv, stream);
+  return launch_typed<T, HKV, NG, kLoaderCpAsync>(prm, mk, mv, stream);
+}
+
+template <typename T, int HKV>
+int launch_group(const Params &prm, bool tma, const CUtensorMap &mk,
+                 const CUtensorMap &mv, void *stream) {
+  constexpr int kQw = kConsumerWarps / HKV;
+  const int gq = (prm.group + kQw - 1) / kQw;
+  if (gq > 8) return launch_loader<T, HKV, 2>(prm, tma, mk, mv, stream);
+  return launch_loader<T, HKV, 1>(prm, tma, mk, mv, stream);
+}
+
 template <typename T>
-int launch_heads(const Params &prm, int hkv, int grid, void *stream) {
+int launch_heads(const Params &prm, int hkv, bool tma, const CUtensorMap &mk,
+                 const CUtensorMap &mv, void *stream) {
   switch (hkv) {
-    case 1: return launch_typed<T, 1>(prm, grid, stream);
-    case 2: return launch_typed<T, 2>(prm, grid, stream);
-    case 4: return launch_typed<T, 4>(prm, grid, stream);
-    default: return launch_typed<T, 8>(prm, grid, stream);
+    case 1: return launch_group<T, 1>(prm, tma, mk, mv, stream);
+    case 2: return launch_group<T, 2>(prm, tma, mk, mv, stream);
+    case 4: return launch_group<T, 4>(prm, tma, mk, mv, stream);
+    default: return launch_group<T, 8>(prm, tma, mk, mv, stream);
   }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// K or V pages viewed as [token row][head][d] with d innermost; boxes of 16
+// token rows x 1 head x 64 elements, 128-byte swizzle.
+bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
+                  int page_size, int hkv) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(hkv),
+                        static_cast<cuuint64_t>(num_pages) * page_size};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBytes),
+                           static_cast<cuuint64_t>(kRowBytes) * hkv};
+  cuuint32_t box[3] = {64, 1, kTile};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(base), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -514,9 +688,19 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   prm.max_partials = a.max_partials;
   prm.image_words = a.image_words;
   prm.grid = a.num_ctas;
+
+  alignas(64) CUtensorMap mk;
+  alignas(64) CUtensorMap mv;
+  std::memset(&mk, 0, sizeof(mk));
+  std::memset(&mv, 0, sizeof(mv));
+  // TMA when every tile lies inside one page and token rows fit in int32
+  const bool tma = a.page_size % kTile == 0 && a.num_pages > 0 &&
+                   a.num_pages * static_cast<long long>(a.page_size) < (1ll << 31) &&
+                   encode_pages(&mk, a.k_pages, a.num_pages, a.page_size, a.num_kv_heads) &&
+                   encode_pages(&mv, a.v_pages, a.num_pages, a.page_size, a.num_kv_heads);
   if (a.dtype == PKD_BF16)
-    return launch_heads<__nv_bfloat16>(prm, a.num_kv_heads, a.num_ctas, stream);
-  return launch_heads<__half>(prm, a.num_kv_heads, a.num_ctas, stream);
+    return launch_heads<__nv_bfloat16>(prm, a.num_kv_heads, tma, mk, mv, stream);
+  return launch_heads<__half>(prm, a.num_kv_heads, tma, mk, mv, stream);
 }
 
 }  // namespace pkd

@@ -60,7 +60,7 @@ PKD_HD inline int64_t partial_slot_floats(int64_t hq, int64_t d) {
 
 constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 16;
-inline int default_tile_tokens(int num_kv_heads) { return 128 / num_kv_heads; }
+constexpr int kTileTokens = 16;  // tokens per decode tile, every Hkv
 
 // Thread-local error message; returns `status` for convenience.
 pkd_status fail(pkd_status status, const std::string &message);

@@ -59,8 +59,8 @@ pkd_status check_problem(const pkd_problem &p, bool need_ctas) {
     return fail(PKD_ERR_UNSUPPORTED, "num_kv_heads must be 1, 2, 4 or 8");
   if (p.num_qo_heads / p.num_kv_heads > kMaxGroup)
     return fail(PKD_ERR_UNSUPPORTED, "query group larger than 16");
-  if (p.tile_tokens != 0 && p.tile_tokens != default_tile_tokens(p.num_kv_heads))
-    return fail(PKD_ERR_UNSUPPORTED, "tile_tokens must be 0 or 128 / Hkv");
+  if (p.tile_tokens != 0 && p.tile_tokens != kTileTokens)
+    return fail(PKD_ERR_UNSUPPORTED, "tile_tokens must be 0 or 16");
   if (need_ctas && p.num_ctas <= 0)
     return fail(PKD_ERR_INVALID_ARG, "num_ctas must be explicit here");
   return PKD_OK;
@@ -95,8 +95,7 @@ pkd_status plan_host_impl(const pkd_problem &in, const int32_t *kv_indptr,
       (in.batch == 0 && !kv_indptr))
     return fail(PKD_ERR_INVALID_ARG, "null pointer");
   pkd_problem p = in;
-  if (p.tile_tokens == 0 && p.num_kv_heads > 0)
-    p.tile_tokens = default_tile_tokens(p.num_kv_heads);
+  if (p.tile_tokens == 0) p.tile_tokens = kTileTokens;
   pkd_status st = check_problem(p, true);
   if (st != PKD_OK) return st;
   const int B = p.batch, P = p.page_size, T = p.tile_tokens, C = p.num_ctas;

@@ -17,13 +17,13 @@ def problem_for(batch, page_size, hkv=8, hq=32, ctas=152, m=1, num_pages=1 << 20
                             tile_tokens=tile, max_batch=max_batch)
 
 
-HKV_FOR_TILE = {16: 8, 32: 4, 64: 2, 128: 1}
+HKV_FOR_CASE = [8, 8, 4, 8, 2, 1, 4, 8, 2]
 
 
-@pytest.mark.parametrize("case", CASES)
-def test_plan_matches_reference_rule(case):
-    batch, page_size, max_len, tile, ctas, m = case
-    hkv = HKV_FOR_TILE[tile]
+@pytest.mark.parametrize("case,hkv", list(zip(CASES, HKV_FOR_CASE)))
+def test_plan_matches_reference_rule(case, hkv):
+    batch, page_size, max_len, _, ctas, m = case
+    tile = 16
     rng = np.random.default_rng(hash(case) % (2 ** 32) + 1)
     for _ in range(3):
         _, indptr, last = random_table(rng, batch, page_size, max_len)
@@ -101,6 +101,7 @@ def test_unsupported_and_invalid_problems():
     expect_status(-4, pkd.plan_host, problem_for(1, 16, hkv=1, hq=32), indptr, last)
     expect_status(-4, pkd.plan_host, problem_for(1, 16, dtype="f32"), indptr, last)
     expect_status(-4, pkd.plan_host, problem_for(1, 16, tile=32), indptr, last)
+    expect_status(-4, pkd.plan_host, problem_for(1, 16, hkv=4, hq=8, tile=32), indptr, last)
     expect_status(-1, pkd.plan_host, problem_for(1, 16, hkv=8, hq=12), indptr, last)
     expect_status(-1, pkd.plan_host, problem_for(2, 16, max_batch=1),
                   np.array([0, 1, 2], np.int32), np.array([3, 3], np.int32))
