@@ -560,6 +560,9 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + loader_warps<LOADER>())
     if (threadIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
     return;
   }
+  // a merge kernel launched after this one may be scheduled from now on; it
+  // waits for this grid to finish before it reads any partial state
+  ptx::launch_dependents();
   if (u_begin == u_end) return;
 
   if (threadIdx.x == 0) {

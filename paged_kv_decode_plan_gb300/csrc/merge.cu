@@ -48,6 +48,10 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int32_t *merge_req = image + o.merge_req;
   const long long slot_floats = partial_slot_floats(hq, kHeadDim);
   const long long rows = static_cast<long long>(num_split) * hq;
+  // launched as a programmatic dependent of the decode kernel: the plan image
+  // was in place before that kernel started, the partial states are only
+  // complete once it has finished
+  ptx::wait_primary_grid();
 
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const int i = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
@@ -195,15 +199,29 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 int launch_merge_partials(const MergePartialsArgs &a, void *stream) {
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // programmatic dependent launch: the grid may be scheduled while the decode
+  // kernel before it on the stream is still running
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  uint16_t *out = static_cast<uint16_t *>(a.out);
+  cudaError_t e;
   if (a.dtype == PKD_BF16)
-    merge_partials_kernel<__nv_bfloat16><<<a.grid, kMergeThreads, 0, st>>>(
-        a.image, a.partials, static_cast<uint16_t *>(a.out), a.lse, a.num_qo_heads,
-        a.batch, a.max_partials, a.image_words);
+    e = cudaLaunchKernelEx(&cfg, merge_partials_kernel<__nv_bfloat16>, a.image,
+                           a.partials, out, a.lse, a.num_qo_heads, a.batch,
+                           a.max_partials, a.image_words);
   else
-    merge_partials_kernel<__half><<<a.grid, kMergeThreads, 0, st>>>(
-        a.image, a.partials, static_cast<uint16_t *>(a.out), a.lse, a.num_qo_heads,
-        a.batch, a.max_partials, a.image_words);
+    e = cudaLaunchKernelEx(&cfg, merge_partials_kernel<__half>, a.image, a.partials,
+                           out, a.lse, a.num_qo_heads, a.batch, a.max_partials,
+                           a.image_words);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
