@@ -215,7 +215,7 @@ class Runner:
     previous step still runs; the decode launch waits only for its own copy.
     """
 
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, kv_loader=0):
         import torch
         import paged_kv_decode_plan_gb300 as pkd
         self.torch = torch
@@ -232,7 +232,8 @@ class Runner:
             prob = pkd.make_problem(batch=t.batch, num_qo_heads=wl.num_qo_heads,
                                     num_kv_heads=wl.num_kv_heads, page_size=t.page_size,
                                     dtype=wl.dtype, num_pages=wl.num_pages,
-                                    min_chunks_per_request=wl.min_chunks_per_request)
+                                    min_chunks_per_request=wl.min_chunks_per_request,
+                                    kv_loader=kv_loader)
             ws = [pkd.Workspace(prob, device=device) for _ in range(2)]
             dev = tuple(torch.from_numpy(a).to(device) for a in
                         (t.kv_indptr, t.kv_indices, t.kv_last_page_len))
@@ -307,14 +308,23 @@ class Runner:
         return int(self.tables[0].lengths().sum()) * per_token
 
 
+def make_workload(args):
+    from paged_kv_decode_plan_gb300 import workloads
+    if args.batch is None:
+        return workloads.WORKLOADS[args.workload]()
+    if args.workload not in ("longctx", "cascade"):
+        raise SystemExit("--batch applies to the longctx and cascade workloads")
+    return workloads.WORKLOADS[args.workload](batch=args.batch)
+
+
 def run_ours(args, ranks):
     import torch
     from paged_kv_decode_plan_gb300 import workloads
 
     torch.cuda.set_device(ranks.local)
     device = torch.device("cuda", ranks.local)
-    wl = workloads.WORKLOADS[args.workload]()
-    runner = Runner(wl, device)
+    wl = make_workload(args)
+    runner = Runner(wl, device, kv_loader={"auto": 0, "tma": 1, "bulk": 2}[args.loader])
     stream = torch.cuda.current_stream()
 
     # host plan time (median of 20)
@@ -391,6 +401,7 @@ def run_ours(args, ranks):
         "plan_host_us": round(statistics.median(plan_times) * 1e6, 1),
         "num_units": runner.parts[0]["plan"].num_units,
         "num_split_requests": runner.parts[0]["plan"].num_split_requests,
+        "kv_loader": args.loader,
         "timing": "pass 1 (value, ms_per_step): K steps between two events; pass 2 "
                   "(decode_us, roofline): the same K steps with events around each "
                   "decode launch",
@@ -504,7 +515,7 @@ def run_reference(args, ranks):
     import oracle
     from paged_kv_decode_plan_gb300 import workloads
     oracle.build()
-    wl = workloads.WORKLOADS[args.workload]()
+    wl = make_workload(args)
     codes = (workloads.as_codes(wl.q), workloads.as_codes(wl.k_pages),
              workloads.as_codes(wl.v_pages))
     t = wl.table
@@ -564,6 +575,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(DESCRIPTIONS), default="batch64")
     ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="smaller batch of the longctx / cascade workload (profiling)")
+    ap.add_argument("--loader", choices=["auto", "tma", "bulk"], default="auto",
+                    help="K/V loader of the decode kernel (auto: bulk rows)")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

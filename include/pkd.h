@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define PKD_ABI_VERSION 1
+#define PKD_ABI_VERSION 2
 
 typedef enum {
   PKD_OK = 0,
@@ -60,6 +60,13 @@ typedef enum {
 } pkd_status;
 
 typedef enum { PKD_F16 = 0, PKD_BF16 = 1, PKD_F32 = 2 } pkd_dtype;
+
+/* How the decode kernel moves K/V pages into shared memory. */
+typedef enum {
+  PKD_LOADER_AUTO = 0,       /* the library's choice: bulk rows */
+  PKD_LOADER_TMA_TILES = 1,  /* TMA tiled loads of 16-token boxes (page_size % 16 == 0) */
+  PKD_LOADER_BULK_ROWS = 2   /* one bulk copy per token row of all heads (any page_size) */
+} pkd_loader;
 
 /* Bits of the device status word (see pkd_check_status). */
 #define PKD_DEVICE_BAD_PAGE 1u    /* a page id outside [0, num_pages) */
@@ -84,6 +91,8 @@ typedef struct {
   int32_t tile_tokens;   /* tokens per pipeline tile; 0 = 16 (the decode
                             kernel's tile); other values are unsupported */
   int32_t max_batch;     /* capacity used to size workspaces; 0 = batch */
+  int32_t kv_loader;     /* pkd_loader */
+  int32_t reserved;      /* 0 */
 } pkd_problem;
 
 /* Result of planning: plain data, owned and stored by the caller. */

@@ -22,6 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkd.so")
 
 PKD_F16, PKD_BF16, PKD_F32 = 0, 1, 2
+LOADER_AUTO, LOADER_TMA_TILES, LOADER_BULK_ROWS = 0, 1, 2
 DEVICE_BAD_PAGE, DEVICE_BAD_LENGTH, DEVICE_BAD_PLAN, DEVICE_TIMEOUT = 1, 2, 4, 8
 STATUS_NAMES = {0: "PKD_OK", -1: "PKD_ERR_INVALID_ARG", -2: "PKD_ERR_PAGE_TABLE",
                 -3: "PKD_ERR_WORKSPACE", -4: "PKD_ERR_UNSUPPORTED",
@@ -46,7 +47,8 @@ class Problem(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("num_pages", ctypes.c_int64), ("num_ctas", ctypes.c_int32),
                 ("min_chunks_per_request", ctypes.c_int32),
-                ("tile_tokens", ctypes.c_int32), ("max_batch", ctypes.c_int32)]
+                ("tile_tokens", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+                ("kv_loader", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -95,7 +97,7 @@ def load():
                  "pkd_run_decode", "pkd_run_merge", "pkd_merge_states",
                  "pkd_check_status", "pkd_run_static"):
         getattr(lib, name).restype = ctypes.c_int
-    if lib.pkd_abi_version() != 1:
+    if lib.pkd_abi_version() != 2:
         raise RuntimeError("libpkd.so ABI version mismatch")
     _lib = lib
     return lib
@@ -121,10 +123,10 @@ def _dtype_code(dtype) -> int:
 
 def make_problem(*, batch, num_qo_heads, num_kv_heads, page_size, dtype,
                  num_pages, head_dim=128, num_ctas=0, min_chunks_per_request=1,
-                 tile_tokens=0, max_batch=0) -> Problem:
+                 tile_tokens=0, max_batch=0, kv_loader=LOADER_AUTO) -> Problem:
     return Problem(batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                    _dtype_code(dtype), num_pages, num_ctas,
-                   min_chunks_per_request, tile_tokens, max_batch)
+                   min_chunks_per_request, tile_tokens, max_batch, kv_loader, 0)
 
 
 def workspace_size(problem: Problem):

@@ -134,7 +134,10 @@ pkd_status pkd_run_decode(const pkd_plan_t *plan, const void *q,
   a.dtype = p.dtype;
   a.max_partials = plan->num_partials;
   a.image_words = static_cast<int>(plan->int_ws_bytes_used / 4);
+  a.loader = p.kv_loader;
   cudaError_t e = static_cast<cudaError_t>(pkd::launch_decode(a, stream));
+  if (e == cudaErrorNotSupported)
+    return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");
   if (e != cudaSuccess) return cuda_fail(e, "launching the decode kernel");
   return PKD_OK;
 }

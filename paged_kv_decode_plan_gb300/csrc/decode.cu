@@ -5,12 +5,13 @@
 // tokens of every key/value head (16 * Hkv * 512 bytes of K and V).
 //
 // Roles inside a CTA:
-//  * loader warp(s) fill a ring of shared-memory stages.  When a page holds
-//    whole 16-token tiles (page_size % 16 == 0) one warp issues TMA tiled
-//    loads (cp.async.bulk.tensor, 128-byte swizzle), one 16 x 64-element box
-//    per (tensor, head, d-half), completing on the stage's "full" mbarrier.
-//    Otherwise four warps copy 16-byte chunks with cp.async into the same
-//    swizzled layout and arrive on the barrier when their copies land.
+//  * one loader warp fills a ring of shared-memory stages.  By default it
+//    issues one 1-D bulk copy (cp.async.bulk) per (tensor, token): in NHD
+//    memory a token's rows of all heads are contiguous, so this works for
+//    any page size.  On request (PKD_LOADER_TMA_TILES), when pages hold
+//    whole 16-token tiles, it issues TMA tiled loads (cp.async.bulk.tensor,
+//    128-byte swizzle), one 16 x 64-element box per (tensor, head, d-half).
+//    Copies complete on the stage's "full" mbarrier.
 //  * eight consumer warps compute.  Warp w owns key/value head
 //    w / (8 / Hkv) and a slice of that head's query group, so no two warps
 //    share an output row.  With the query group as the N = 8 side of
@@ -40,6 +41,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -55,22 +57,32 @@ constexpr int kConsumerWarps = 8;
 constexpr int kTile = 16;                           // tokens per tile
 constexpr int kRowBytes = kHeadDim * 2;             // one token, one head
 constexpr int kHalfBytes = kTile * 128;             // 16 rows x 64 elements
-constexpr int kStageBudget = 3 * 64 * 1024;         // bytes of stages per CTA
+constexpr int kStageBudget = 200 * 1024;            // bytes of stages per CTA
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLazy = 8.f;                        // log2 of the largest p
 constexpr long long kWaitPolls = 1ll << 22;         // bounded mbarrier waits
 
-enum Loader : int { kLoaderTma = 0, kLoaderCpAsync = 1 };
+enum Loader : int { kLoaderTma = PKD_LOADER_TMA_TILES, kLoaderBulk = PKD_LOADER_BULK_ROWS };
 
-template <int L>
-__host__ __device__ constexpr int loader_warps() { return L == kLoaderTma ? 1 : 4; }
-__host__ __device__ constexpr int head_bytes() { return 2 * kHalfBytes; }  // one head
-template <int HKV>
-__host__ __device__ constexpr int tensor_bytes() { return HKV * head_bytes(); }
-template <int HKV>
-__host__ __device__ constexpr int stage_bytes() { return 2 * tensor_bytes<HKV>(); }
-template <int HKV>
-__host__ __device__ constexpr int num_stages() { return kStageBudget / stage_bytes<HKV>(); }
+// Shared-memory geometry of one stage (K tile, then V tile) for a loader.
+//  * TMA tiled loader: per head [d-half][16 rows][128 B], 16-byte chunks
+//    XOR-swizzled by row (the TMA 128-byte swizzle).
+//  * bulk loader: token rows of Hkv * 256 bytes (all heads, as in NHD memory)
+//    at a stride of Hkv * 256 + 16 bytes, so that eight consecutive rows fall
+//    on eight different 16-byte bank groups.
+template <int HKV, int L>
+struct Geometry {
+  static constexpr bool kPadded = L == kLoaderBulk;
+  static constexpr int kLoaderWarps = 1;
+  static constexpr int kRowStride = HKV * kRowBytes + 16;
+  static constexpr int kHeadBytes = 2 * kHalfBytes;
+  static constexpr int kTensorBytes = kPadded ? kTile * kRowStride : HKV * kHeadBytes;
+  static constexpr int kStageBytes = 2 * kTensorBytes;
+  static constexpr int kStages = kStageBudget / kStageBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 16 * kStages + 16;
+  static_assert(kStages >= 2, "at least two stages");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
 
 struct Params {
   const uint16_t *q, *k, *v;
@@ -157,6 +169,14 @@ __device__ __forceinline__ uint32_t tile_offset(int r, int c) {
   return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
+// Offset of chunk c of token row r of head h within a stage's K (or V) tile.
+template <int HKV, int L>
+__device__ __forceinline__ uint32_t kv_offset(int h, int r, int c) {
+  using G = Geometry<HKV, L>;
+  if (G::kPadded) return r * G::kRowStride + h * kRowBytes + (c << 4);
+  return h * G::kHeadBytes + tile_offset(r, c);
+}
+
 // ----------------------------------------------------------------- loaders
 
 template <int HKV>
@@ -164,7 +184,8 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
                          const CUtensorMap *map_v, const int32_t *units,
                          int num_partials, int u_begin, int u_end, uint8_t *stages,
                          uint32_t full0, uint32_t empty0, volatile int *abort) {
-  constexpr int kStages = num_stages<HKV>();
+  using G = Geometry<HKV, kLoaderTma>;
+  constexpr int kStages = G::kStages;
   const int lane = threadIdx.x & 31;
   const uint32_t stage0 = ptx::smem_u32(stages);
   int it = 0;
@@ -188,15 +209,14 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
         if (lane == 0) flag(p.image, PKD_DEVICE_BAD_PAGE);
         page = 0;
       }
-      if (lane == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes<HKV>());
+      if (lane == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, G::kStageBytes);
       __syncwarp();
       if (lane < 4 * HKV) {
         const int tensor = lane / (2 * HKV);
         const int head = (lane >> 1) % HKV;
         const int half = lane & 1;
-        const uint32_t dst = stage0 + s * stage_bytes<HKV>() +
-                             tensor * tensor_bytes<HKV>() + head * head_bytes() +
-                             half * kHalfBytes;
+        const uint32_t dst = stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
+                             head * G::kHeadBytes + half * kHalfBytes;
         ptx::tma_load_3d(dst, tensor ? map_v : map_k, half * 64, head,
                          page * p.page_size + slot0, full0 + 8 * s);
       }
@@ -208,33 +228,27 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
     wait_phase(full0 + 8 * (j % kStages), (j / kStages) & 1, abort, true);
 }
 
+// One 1-D bulk copy per (tensor, token) row: lane l moves row l & 15 of K
+// (l < 16) or V (l >= 16); page ids are loaded one tile ahead.
 template <int HKV>
-struct CpAsyncLoader {
-  static constexpr int kRows = 2 * HKV;  // (token, head) rows per thread per tensor
+__device__ void load_bulk(const Params &p, const int32_t *units, int num_partials,
+                          int u_begin, int u_end, uint8_t *stages, uint32_t full0,
+                          uint32_t empty0, volatile int *abort) {
+  using G = Geometry<HKV, kLoaderBulk>;
+  constexpr int kStages = G::kStages;
+  constexpr uint32_t kRow = HKV * kRowBytes;  // bytes of one token, all heads
+  const int lane = threadIdx.x & 31;
+  const int tensor = lane >> 4, r = lane & 15;
+  const uint16_t *base = tensor ? p.v : p.k;
+  const uint32_t stage0 = ptx::smem_u32(stages);
 
-  const Params &p;
-  const int32_t *units;
-  int num_partials, u, u_end, t;
+  // cursor over the CTA's tiles; (tok0, t1, page, slot) describe the next one
+  int u = u_begin, t = 0;
   Unit unit;
-  bool have;
-  int tok0, t1;
-  int page[kRows], slot[kRows];
-
-  __device__ CpAsyncLoader(const Params &p_, const int32_t *units_, int np, int ub,
-                           int ue)
-      : p(p_), units(units_), num_partials(np), u(ub), u_end(ue), t(0), have(false) {
-    if (u < u_end) unit = read_unit(p, units, u, num_partials);
-    describe();
-  }
-
-  __device__ __forceinline__ static int lt() {
-    return static_cast<int>(threadIdx.x) - 32 * kConsumerWarps;
-  }
-  __device__ __forceinline__ static int row_token(int j) { return ((lt() >> 4) + 8 * j) / HKV; }
-  __device__ __forceinline__ static int row_head(int j) { return ((lt() >> 4) + 8 * j) % HKV; }
-
-  // Moves to the next tile and starts the page-id loads it needs.
-  __device__ void describe() {
+  if (u < u_end) unit = read_unit(p, units, u, num_partials);
+  int tok0 = 0, t1 = 0, page = 0, slot = 0;
+  bool have = false;
+  auto describe = [&]() {
     while (u < u_end && unit.t0 + t * kTile >= unit.t1) {
       ++u;
       t = 0;
@@ -244,75 +258,56 @@ struct CpAsyncLoader {
     if (!have) return;
     tok0 = unit.t0 + t * kTile;
     t1 = unit.t1;
-#pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      const int tok = tok0 + row_token(j);
-      int pg = 0, sl = 0;
-      if (tok < t1) {
-        const int pi = tok / p.page_size;
-        sl = tok - pi * p.page_size;
-        pg = __ldg(p.indices + unit.pbase + pi);
-      }
-      page[j] = pg;
-      slot[j] = sl;
+    const int tok = tok0 + r;
+    page = 0;
+    slot = 0;
+    if (tok < t1) {
+      const int pi = tok / p.page_size;
+      slot = tok - pi * p.page_size;
+      page = __ldg(p.indices + unit.pbase + pi);
     }
     ++t;
-  }
+  };
+  describe();
 
-  // Copies the described tile into the stage at `dst` (zero rows past the
-  // unit's end).
-  __device__ void issue(uint32_t dst) {
-    const int c = lt() & 15;
-#pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      const int tl = row_token(j);
-      const int head = row_head(j);
-      bool valid = tok0 + tl < t1;
-      if (valid && static_cast<unsigned long long>(page[j]) >=
-                       static_cast<unsigned long long>(p.num_pages)) {
-        flag(p.image, PKD_DEVICE_BAD_PAGE);
-        valid = false;
-      }
-      const long long row =
-          valid ? (static_cast<long long>(page[j]) * p.page_size + slot[j]) * HKV + head
-                : 0;
-      const uint32_t off = head * head_bytes() + tile_offset(tl, c);
-      const uint32_t n = valid ? 16u : 0u;
-      ptx::cp_async_16(dst + off, p.k + row * kHeadDim + c * 8, n);
-      ptx::cp_async_16(dst + tensor_bytes<HKV>() + off, p.v + row * kHeadDim + c * 8, n);
-    }
-  }
-};
-
-template <int HKV>
-__device__ void load_cp_async(const Params &p, const int32_t *units, int num_partials,
-                              int u_begin, int u_end, uint8_t *stages, uint32_t full0,
-                              uint32_t empty0, volatile int *abort) {
-  constexpr int kStages = num_stages<HKV>();
-  const uint32_t stage0 = ptx::smem_u32(stages);
-  CpAsyncLoader<HKV> ld(p, units, num_partials, u_begin, u_end);
   int it = 0;
-  while (ld.have) {
+  while (have) {
     const int s = it % kStages;
     if (!wait_phase(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, abort)) {
-      give_up(p, abort);
+      if (lane == 0) give_up(p, abort);
       break;
     }
-    ld.issue(stage0 + s * stage_bytes<HKV>());
-    ptx::cp_async_mbar_arrive_noinc(full0 + 8 * s);
-    ld.describe();
+    const int nvalid = min(kTile, t1 - tok0);
+    if (lane == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, 2u * nvalid * kRow);
+    __syncwarp();
+    if (r < nvalid) {
+      int pg = page;
+      if (static_cast<unsigned long long>(pg) >=
+          static_cast<unsigned long long>(p.num_pages)) {
+        flag(p.image, PKD_DEVICE_BAD_PAGE);
+        pg = 0;
+      }
+      const uint16_t *src =
+          base + (static_cast<long long>(pg) * p.page_size + slot) * HKV * kHeadDim;
+      ptx::bulk_load(stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
+                         r * G::kRowStride,
+                     src, kRow, full0 + 8 * s);
+    }
+    describe();
     ++it;
   }
-  ptx::cp_async_wait_all();
+  for (int j = max(0, it - kStages); j < it; ++j)
+    wait_phase(full0 + 8 * (j % kStages), (j / kStages) & 1, abort, true);
 }
 
 // ---------------------------------------------------------------- consumer
 
-template <typename T, int HKV, int NG>
+template <typename T, int HKV, int NG, int L>
 __device__ void consume(const Params &p, const int32_t *units, int num_partials,
                         int u_begin, int u_end, const uint8_t *stages, uint32_t full0,
                         uint32_t empty0, volatile int *abort) {
-  constexpr int kStages = num_stages<HKV>();
+  using G = Geometry<HKV, L>;
+  constexpr int kStages = G::kStages;
   constexpr int kQw = kConsumerWarps / HKV;       // warps per key/value head
   constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -372,8 +367,8 @@ __device__ void consume(const Params &p, const int32_t *units, int num_partials,
         stop = true;
         break;
       }
-      const uint32_t kb = stage0 + s * stage_bytes<HKV>() + hk * head_bytes();
-      const uint32_t vb = kb + tensor_bytes<HKV>();
+      const uint32_t kb = stage0 + s * G::kStageBytes;
+      const uint32_t vb = kb + G::kTensorBytes;
       const int valid = min(kTile, unit.t1 - unit.t0 - t * kTile);
 
       // S^T = K Q^T: rows are tokens, columns this warp's query heads
@@ -383,7 +378,8 @@ __device__ void consume(const Params &p, const int32_t *units, int num_partials,
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         uint32_t a[4];
-        ptx::ldmatrix_x4(kb + tile_offset(a_row, 2 * kk + a_hi), a[0], a[1], a[2], a[3]);
+        ptx::ldmatrix_x4(kb + kv_offset<HKV, L>(hk, a_row, 2 * kk + a_hi), a[0], a[1],
+                         a[2], a[3]);
 #pragma unroll
         for (int n = 0; n < NG; ++n) ptx::mma_16816<T>(sc[n], a, qb[n][kk][0], qb[n][kk][1]);
       }
@@ -462,8 +458,8 @@ __device__ void consume(const Params &p, const int32_t *units, int num_partials,
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t a[4];
-        ptx::ldmatrix_x4_trans(vb + tile_offset(v_row, 2 * mt + v_hi), a[0], a[1], a[2],
-                               a[3]);
+        ptx::ldmatrix_x4_trans(vb + kv_offset<HKV, L>(hk, v_row, 2 * mt + v_hi), a[0],
+                               a[1], a[2], a[3]);
         a[0] &= m01;
         a[1] &= m01;
         a[2] &= m89;
@@ -526,15 +522,16 @@ __device__ void consume(const Params &p, const int32_t *units, int num_partials,
 // ------------------------------------------------------------------ kernel
 
 template <typename T, int HKV, int NG, int LOADER>
-__global__ void __launch_bounds__(32 * (kConsumerWarps + loader_warps<LOADER>()), 1)
+__global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::kLoaderWarps), 1)
     decode_kernel(const __grid_constant__ Params p,
                   const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v) {
-  constexpr int kStages = num_stages<HKV>();
+  using G = Geometry<HKV, LOADER>;
+  constexpr int kStages = G::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *stages = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(stages + kStages * stage_bytes<HKV>());
+  uint64_t *bars = reinterpret_cast<uint64_t *>(stages + kStages * G::kStageBytes);
   volatile int *abort = reinterpret_cast<volatile int *>(bars + 2 * kStages);
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages;
@@ -566,8 +563,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + loader_warps<LOADER>())
   if (u_begin == u_end) return;
 
   if (threadIdx.x == 0) {
-    const uint32_t full_count =
-        LOADER == kLoaderTma ? 1u : 32u * loader_warps<kLoaderCpAsync>();
+    const uint32_t full_count = 1u;  // the loader's arrive.expect_tx
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full0 + 8 * s, full_count);
       ptx::mbar_init(empty0 + 8 * s, kConsumerWarps);
@@ -583,56 +579,61 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + loader_warps<LOADER>())
       load_tma<HKV>(p, &map_k, &map_v, units, num_partials, u_begin, u_end, stages,
                     full0, empty0, abort);
     else
-      load_cp_async<HKV>(p, units, num_partials, u_begin, u_end, stages, full0,
-                         empty0, abort);
+      load_bulk<HKV>(p, units, num_partials, u_begin, u_end, stages, full0, empty0,
+                     abort);
   } else {
-    consume<T, HKV, NG>(p, units, num_partials, u_begin, u_end, stages, full0,
-                        empty0, abort);
+    consume<T, HKV, NG, LOADER>(p, units, num_partials, u_begin, u_end, stages, full0,
+                                empty0, abort);
   }
 }
 
-template <int HKV>
-__host__ __device__ constexpr int smem_bytes() {
-  return 1024 + num_stages<HKV>() * stage_bytes<HKV>() + 16 * num_stages<HKV>() + 16;
-}
+constexpr int kMaxDevices = 64;
 
 template <typename T, int HKV, int NG, int LOADER>
 int launch_typed(const Params &prm, const CUtensorMap &mk, const CUtensorMap &mv,
                  void *stream) {
+  using G = Geometry<HKV, LOADER>;
   auto kernel = decode_kernel<T, HKV, NG, LOADER>;
-  const int smem = smem_bytes<HKV>();
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = G::kSmemBytes;
+  // the dynamic shared-memory limit is raised once per device
+  static std::atomic<bool> raised[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  kernel<<<prm.grid, 32 * (kConsumerWarps + loader_warps<LOADER>()), smem,
+  if (dev < 0 || dev >= kMaxDevices || !raised[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) raised[dev].store(true, std::memory_order_release);
+  }
+  kernel<<<prm.grid, 32 * (kConsumerWarps + G::kLoaderWarps), smem,
            static_cast<cudaStream_t>(stream)>>>(prm, mk, mv);
   return cudaGetLastError();
 }
 
 template <typename T, int HKV, int NG>
-int launch_loader(const Params &prm, bool tma, const CUtensorMap &mk,
+int launch_loader(const Params &prm, int loader, const CUtensorMap &mk,
                   const CUtensorMap &mv, void *stream) {
-  if (tma) return launch_typed<T, HKV, NG, kLoaderTma>(prm, mk, mv, stream);
-  return launch_typed<T, HKV, NG, kLoaderCpAsync>(prm, mk, mv, stream);
+  if (loader == kLoaderTma) return launch_typed<T, HKV, NG, kLoaderTma>(prm, mk, mv, stream);
+  return launch_typed<T, HKV, NG, kLoaderBulk>(prm, mk, mv, stream);
 }
 
 template <typename T, int HKV>
-int launch_group(const Params &prm, bool tma, const CUtensorMap &mk,
+int launch_group(const Params &prm, int loader, const CUtensorMap &mk,
                  const CUtensorMap &mv, void *stream) {
   constexpr int kQw = kConsumerWarps / HKV;
   const int gq = (prm.group + kQw - 1) / kQw;
-  if (gq > 8) return launch_loader<T, HKV, 2>(prm, tma, mk, mv, stream);
-  return launch_loader<T, HKV, 1>(prm, tma, mk, mv, stream);
+  if (gq > 8) return launch_loader<T, HKV, 2>(prm, loader, mk, mv, stream);
+  return launch_loader<T, HKV, 1>(prm, loader, mk, mv, stream);
 }
 
 template <typename T>
-int launch_heads(const Params &prm, int hkv, bool tma, const CUtensorMap &mk,
+int launch_heads(const Params &prm, int hkv, int loader, const CUtensorMap &mk,
                  const CUtensorMap &mv, void *stream) {
   switch (hkv) {
-    case 1: return launch_group<T, 1>(prm, tma, mk, mv, stream);
-    case 2: return launch_group<T, 2>(prm, tma, mk, mv, stream);
-    case 4: return launch_group<T, 4>(prm, tma, mk, mv, stream);
-    default: return launch_group<T, 8>(prm, tma, mk, mv, stream);
+    case 1: return launch_group<T, 1>(prm, loader, mk, mv, stream);
+    case 2: return launch_group<T, 2>(prm, loader, mk, mv, stream);
+    case 4: return launch_group<T, 4>(prm, loader, mk, mv, stream);
+    default: return launch_group<T, 8>(prm, loader, mk, mv, stream);
   }
 }
 
@@ -668,6 +669,44 @@ bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of the last page pools seen (encoding is pure host work, but a
+// serving loop passes the same pools on every step).
+bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const DecodeArgs &a) {
+  struct Entry {
+    const void *k, *v;
+    long long num_pages;
+    int page_size, hkv;
+    alignas(64) CUtensorMap mk;
+    alignas(64) CUtensorMap mv;
+  };
+  static std::mutex mutex;
+  static Entry cache[8];
+  static int next = 0;
+  std::lock_guard<std::mutex> lock(mutex);
+  for (const Entry &e : cache)
+    if (e.k == a.k_pages && e.v == a.v_pages && e.num_pages == a.num_pages &&
+        e.page_size == a.page_size && e.hkv == a.num_kv_heads && e.k) {
+      *mk = e.mk;
+      *mv = e.mv;
+      return true;
+    }
+  Entry &e = cache[next];
+  if (!encode_pages(&e.mk, a.k_pages, a.num_pages, a.page_size, a.num_kv_heads) ||
+      !encode_pages(&e.mv, a.v_pages, a.num_pages, a.page_size, a.num_kv_heads)) {
+    e.k = nullptr;
+    return false;
+  }
+  e.k = a.k_pages;
+  e.v = a.v_pages;
+  e.num_pages = a.num_pages;
+  e.page_size = a.page_size;
+  e.hkv = a.num_kv_heads;
+  next = (next + 1) % 8;
+  *mk = e.mk;
+  *mv = e.mv;
+  return true;
+}
+
 }  // namespace
 
 int launch_decode(const DecodeArgs &a, void *stream) {
@@ -696,14 +735,19 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   alignas(64) CUtensorMap mv;
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
-  // TMA when every tile lies inside one page and token rows fit in int32
-  const bool tma = a.page_size % kTile == 0 && a.num_pages > 0 &&
-                   a.num_pages * static_cast<long long>(a.page_size) < (1ll << 31) &&
-                   encode_pages(&mk, a.k_pages, a.num_pages, a.page_size, a.num_kv_heads) &&
-                   encode_pages(&mv, a.v_pages, a.num_pages, a.page_size, a.num_kv_heads);
+  // bulk rows unless TMA tiles were asked for; TMA tiles need every tile
+  // inside one page and token rows that fit in int32
+  int loader = kLoaderBulk;
+  if (a.loader == PKD_LOADER_TMA_TILES) {
+    if (a.page_size % kTile != 0 || a.num_pages <= 0 ||
+        a.num_pages * static_cast<long long>(a.page_size) >= (1ll << 31) ||
+        !cached_maps(&mk, &mv, a))
+      return cudaErrorNotSupported;
+    loader = kLoaderTma;
+  }
   if (a.dtype == PKD_BF16)
-    return launch_heads<__nv_bfloat16>(prm, a.num_kv_heads, tma, mk, mv, stream);
-  return launch_heads<__half>(prm, a.num_kv_heads, tma, mk, mv, stream);
+    return launch_heads<__nv_bfloat16>(prm, a.num_kv_heads, loader, mk, mv, stream);
+  return launch_heads<__half>(prm, a.num_kv_heads, loader, mk, mv, stream);
 }
 
 }  // namespace pkd

@@ -93,6 +93,7 @@ struct DecodeArgs {
   int64_t num_pages;
   int batch, num_qo_heads, num_kv_heads, page_size, num_ctas, dtype;
   int max_partials, image_words;
+  int loader;  // pkd_loader of the problem
 };
 int launch_decode(const DecodeArgs &a, void *stream);
 

@@ -1,5 +1,5 @@
-// Thin inline-PTX wrappers used by the kernels (PTX ISA: cp.async, ldmatrix,
-// mma.sync m16n8k16, cvt packing, mbarrier, cp.async.bulk.tensor, movmatrix,
+// Thin inline-PTX wrappers used by the kernels (PTX ISA: ldmatrix, mma.sync
+// m16n8k16, cvt packing, mbarrier, cp.async.bulk(.tensor), movmatrix,
 // griddepcontrol).  sm_103a only.
 #pragma once
 
@@ -12,24 +12,6 @@ namespace ptx {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// 16-byte global->shared async copy; src_bytes = 0 writes 16 zero bytes and
-// reads nothing.  .cg: cached in L2 only.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src,
-                                            uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
-               "l"(src), "r"(src_bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 // Four 8x8 b16 matrices; lane l supplies the row address of matrix l / 8.
@@ -148,17 +130,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Arrive on `bar` once all of this thread's prior cp.async copies land
-// (the barrier's expected count already includes this arrival).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;\n" ::: "memory");
-}
-
 // ---- TMA: 3-D tiled tensor load, completion counted on an mbarrier -----
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tensor_map,
@@ -167,6 +138,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tensor_map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// ---- TMA: 1-D bulk copy global -> shared, completion on an mbarrier ------
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

@@ -41,7 +41,7 @@ class DeviceBatch:
 
 
 def run_pkd(dev: DeviceBatch, table=None, *, num_ctas=0, min_chunks=None,
-            sm_scale=None, ws=None, q=None):
+            sm_scale=None, ws=None, q=None, kv_loader=0):
     wl = dev.wl
     table = wl.table if table is None else table
     prob = pkd.make_problem(
@@ -49,7 +49,7 @@ def run_pkd(dev: DeviceBatch, table=None, *, num_ctas=0, min_chunks=None,
         page_size=table.page_size, dtype=wl.dtype, num_pages=wl.num_pages,
         num_ctas=num_ctas,
         min_chunks_per_request=wl.min_chunks_per_request if min_chunks is None
-        else min_chunks)
+        else min_chunks, kv_loader=kv_loader)
     ws = ws or pkd.Workspace(prob)
     plan = ws.plan(table.kv_indptr, table.kv_last_page_len, table.kv_indices)
     indptr, indices, last = device_table(table)

@@ -25,11 +25,11 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version():
-    assert pkd.abi_version() == 1
+    assert pkd.abi_version() == 2
 
 
 def test_struct_sizes_match_c_layout():
-    # pkd_problem: 6 x int32, int64, 4 x int32 ; pkd_plan_t: problem + 4 x
+    # pkd_problem: 6 x int32, int64, 6 x int32 ; pkd_plan_t: problem + 4 x
     # int32 + 3 x int64 + 2 x int32
-    assert ctypes.sizeof(pkd.Problem) == 48
-    assert ctypes.sizeof(pkd.Plan) == 96
+    assert ctypes.sizeof(pkd.Problem) == 56
+    assert ctypes.sizeof(pkd.Plan) == 104

@@ -175,6 +175,34 @@ def test_head_layouts(hkv, hq, page):
         gh.compare(out, lse, ref_out, ref_lse, wl.dtype)
 
 
+@pytest.mark.parametrize("page,dtype", [(16, "f16"), (64, "bf16"), (32, "f16")])
+def test_both_loaders_match_the_oracle(page, dtype):
+    # TMA tiled boxes and per-token bulk rows on the same pages
+    lengths = [5, 1000, 0, 64, 333, 2048, 16]
+    used = sum((n + page - 1) // page for n in lengths)
+    wl = workloads.make_paged("loaders", lengths, num_qo_heads=32, num_kv_heads=8,
+                              page_size=page, dtype=dtype, seed=page, pool_pages=used + 7)
+    dev = gh.DeviceBatch(wl)
+    ref_out, ref_lse = gh.oracle_ref(wl)
+    outs = []
+    for loader in (pkd.LOADER_TMA_TILES, pkd.LOADER_BULK_ROWS):
+        out, lse, _, _, status = gh.run_pkd(dev, num_ctas=40, kv_loader=loader)
+        assert status == 0
+        gh.compare(out, lse, ref_out, ref_lse, wl.dtype)
+        outs.append((out, lse))
+    # same tiles, same arithmetic: the two loaders agree bit for bit
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_tma_loader_refuses_partial_tile_pages():
+    prob = pkd.make_problem(batch=1, num_qo_heads=8, num_kv_heads=8, page_size=8,
+                            dtype="f16", num_pages=4, num_ctas=4,
+                            kv_loader=pkd.LOADER_TMA_TILES)
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.plan_host(prob, np.array([0, 1], np.int32), np.array([3], np.int32))
+    assert e.value.status == -4
+
+
 def test_plan_reuse_is_deterministic():
     wl = workloads.make_paged("reuse", [900, 33, 4000], num_qo_heads=32,
                               num_kv_heads=8, page_size=16, dtype="f16", seed=3)
