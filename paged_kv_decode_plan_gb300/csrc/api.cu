@@ -167,10 +167,9 @@ pkd_status pkd_run_merge(const pkd_plan_t *plan, const void *int_ws_dev,
   m.batch = p.batch;
   m.max_partials = plan->num_partials;
   m.image_words = static_cast<int>(plan->int_ws_bytes_used / 4);
-  const long long rows =
-      static_cast<long long>(plan->num_split_requests) * p.num_qo_heads;
-  const long long cap = 8LL * p.num_ctas;
-  m.grid = static_cast<int>(rows < cap ? rows : cap);
+  m.num_partials = plan->num_partials;
+  m.num_split = plan->num_split_requests;
+  m.grid = 4 * p.num_ctas;  // upper bound on CTAs; rows loop inside
   cudaError_t e = static_cast<cudaError_t>(pkd::launch_merge_partials(m, stream));
   if (e != cudaSuccess) return cuda_fail(e, "launching the merge kernel");
   return PKD_OK;

@@ -21,17 +21,24 @@ namespace {
 constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = 32 * kMergeWarps;
 
-// Split-KV merge: one CTA per (split request, query head) row at a time; the
-// 8 warps take interleaved partial slots, lane l owns d = 4l .. 4l + 3.
-template <typename T>
+// Split-KV merge.  A (split request, query head) row is handled by WPR warps
+// (1, 2, 4 or 8, chosen from the average number of partial states per split
+// request); each warp folds its share of the row's partial states in one
+// online pass (running maximum, rescale when it grows; four states' loads in
+// flight per step), lane l owning d = 4l .. 4l + 3, and the row's warps are
+// combined through shared memory by the same rule.
+template <typename T, int WPR>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_partials_kernel(const int32_t *image, const float *partials,
                           uint16_t *out, float *lse, int hq, int batch,
                           int max_partials, int image_words) {
+  constexpr int kRowsPerCta = kMergeWarps / WPR;
+  constexpr int kUnroll = 4;
   __shared__ float4 red_acc[kMergeWarps][32];
   __shared__ float red_w[kMergeWarps];
   __shared__ float red_m[kMergeWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slot_in_cta = warp / WPR, sub = warp % WPR;
   const int num_ctas = image[kHNumCtas];
   const int num_units = image[kHNumUnits];
   const int num_split = image[kHNumSplit];
@@ -53,66 +60,97 @@ __global__ void __launch_bounds__(kMergeThreads)
   // complete once it has finished
   ptx::wait_primary_grid();
 
-  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
-    const int i = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
-    const int b = merge_req[i];
-    if (b < 0 || b >= batch) continue;
-    const int s0 = max(0, merge_indptr[i]);
-    const int s1 = min(num_partials, merge_indptr[i + 1]);
-
-    // pass 1: largest partial lse
-    float mx = -INFINITY;
-    for (int j = s0 + tid; j < s1; j += kMergeThreads)
-      mx = fmaxf(mx, partials[j * slot_floats + hq * kHeadDim + h]);
-#pragma unroll
-    for (int off = 16; off; off >>= 1)
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red_m[warp] = mx;
-    __syncthreads();
-    mx = red_m[0];
-#pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) mx = fmaxf(mx, red_m[w]);
-    const float ref = mx == -INFINITY ? 0.f : mx;
-
-    // pass 2: weighted sum of the partial outputs
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-#pragma unroll 4
-    for (int j = s0 + warp; j < s1; j += kMergeWarps) {
-      const float *base = partials + j * slot_floats;
-      const float w = expf(base[hq * kHeadDim + h] - ref);
-      const float4 v = reinterpret_cast<const float4 *>(base + h * kHeadDim)[lane];
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
-      wsum += w;
+  for (long long first = static_cast<long long>(blockIdx.x) * kRowsPerCta; first < rows;
+       first += static_cast<long long>(gridDim.x) * kRowsPerCta) {
+    const long long row = first + slot_in_cta;
+    int b = -1, h = 0, s0 = 0, s1 = 0;
+    if (row < rows) {
+      const int i = static_cast<int>(row / hq);
+      h = static_cast<int>(row % hq);
+      b = merge_req[i];
+      s0 = max(0, merge_indptr[i]);
+      s1 = min(num_partials, merge_indptr[i + 1]);
+      if (b < 0 || b >= batch) b = -1;
     }
-    red_acc[warp][lane] = acc;
-    if (lane == 0) red_w[warp] = wsum;
-    __syncthreads();
-    if (warp == 0) {
-      float4 t = red_acc[0][lane];
-      float ws = red_w[0];
+    float m = -INFINITY, ws = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (b >= 0) {
+      for (int j = s0 + sub; j < s1; j += kUnroll * WPR) {
+        float sv[kUnroll];
+        float4 ov[kUnroll];
 #pragma unroll
-      for (int w = 1; w < kMergeWarps; ++w) {
-        const float4 r = red_acc[w][lane];
-        t.x += r.x;
-        t.y += r.y;
-        t.z += r.z;
-        t.w += r.w;
-        ws += red_w[w];
+        for (int k = 0; k < kUnroll; ++k) {
+          const int jj = j + k * WPR;
+          sv[k] = -INFINITY;
+          ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (jj < s1) {
+            const float *base = partials + jj * slot_floats;
+            sv[k] = base[hq * kHeadDim + h];
+            ov[k] = reinterpret_cast<const float4 *>(base + h * kHeadDim)[lane];
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+          if (sv[k] > m) {  // new maximum: rescale what was folded so far
+            const float f = m == -INFINITY ? 0.f : expf(m - sv[k]);
+            acc.x *= f;
+            acc.y *= f;
+            acc.z *= f;
+            acc.w *= f;
+            ws *= f;
+            m = sv[k];
+          }
+          const float w = sv[k] == -INFINITY ? 0.f : expf(sv[k] - m);
+          acc.x += w * ov[k].x;
+          acc.y += w * ov[k].y;
+          acc.z += w * ov[k].z;
+          acc.w += w * ov[k].w;
+          ws += w;
+        }
       }
+    }
+    if (WPR > 1) {
+      red_acc[warp][lane] = acc;
+      if (lane == 0) {
+        red_m[warp] = m;
+        red_w[warp] = ws;
+      }
+      __syncthreads();
+      if (sub == 0 && b >= 0) {
+        float mm = m;
+#pragma unroll
+        for (int w = 1; w < WPR; ++w) mm = fmaxf(mm, red_m[warp + w]);
+        const float f0 = m == -INFINITY ? 0.f : expf(m - mm);
+        acc.x *= f0;
+        acc.y *= f0;
+        acc.z *= f0;
+        acc.w *= f0;
+        ws *= f0;
+#pragma unroll
+        for (int w = 1; w < WPR; ++w) {
+          const float mw = red_m[warp + w];
+          const float f = mw == -INFINITY ? 0.f : expf(mw - mm);
+          const float4 r = red_acc[warp + w][lane];
+          acc.x += f * r.x;
+          acc.y += f * r.y;
+          acc.z += f * r.z;
+          acc.w += f * r.w;
+          ws += f * red_w[warp + w];
+        }
+        m = mm;
+      }
+    }
+    if (sub == 0 && b >= 0) {
       const float inv = ws > 0.f ? 1.f / ws : 0.f;
       uint16_t *dst = out + (static_cast<long long>(b) * hq + h) * kHeadDim + 4 * lane;
       uint2 packed;
-      packed.x = ptx::pack2<T>(t.x * inv, t.y * inv);
-      packed.y = ptx::pack2<T>(t.z * inv, t.w * inv);
+      packed.x = ptx::pack2<T>(acc.x * inv, acc.y * inv);
+      packed.y = ptx::pack2<T>(acc.z * inv, acc.w * inv);
       *reinterpret_cast<uint2 *>(dst) = packed;
       if (lane == 0)
-        lse[static_cast<long long>(b) * hq + h] = ws > 0.f ? ref + logf(ws) : -INFINITY;
+        lse[static_cast<long long>(b) * hq + h] = ws > 0.f ? m + logf(ws) : -INFINITY;
     }
-    __syncthreads();
+    if (WPR > 1) __syncthreads();
   }
 }
 
@@ -196,6 +234,27 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+template <typename T, int WPR>
+cudaError_t launch_merge_wpr(const MergePartialsArgs &a, cudaLaunchConfig_t *cfg) {
+  constexpr int kRowsPerCta = kMergeWarps / WPR;
+  const long long rows = static_cast<long long>(a.num_split) * a.num_qo_heads;
+  const long long want = (rows + kRowsPerCta - 1) / kRowsPerCta;
+  cfg->gridDim = dim3(static_cast<unsigned>(want < a.grid ? want : a.grid));
+  return cudaLaunchKernelEx(cfg, merge_partials_kernel<T, WPR>, a.image, a.partials,
+                            static_cast<uint16_t *>(a.out), a.lse, a.num_qo_heads,
+                            a.batch, a.max_partials, a.image_words);
+}
+
+template <typename T>
+cudaError_t launch_merge_typed(const MergePartialsArgs &a, cudaLaunchConfig_t *cfg) {
+  // warps per row from the average number of partial states per split request
+  const int avg = a.num_split > 0 ? (a.num_partials + a.num_split - 1) / a.num_split : 1;
+  if (avg <= 8) return launch_merge_wpr<T, 1>(a, cfg);
+  if (avg <= 16) return launch_merge_wpr<T, 2>(a, cfg);
+  if (avg <= 32) return launch_merge_wpr<T, 4>(a, cfg);
+  return launch_merge_wpr<T, 8>(a, cfg);
+}
+
 }  // namespace
 
 int launch_merge_partials(const MergePartialsArgs &a, void *stream) {
@@ -205,22 +264,13 @@ int launch_merge_partials(const MergePartialsArgs &a, void *stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  uint16_t *out = static_cast<uint16_t *>(a.out);
-  cudaError_t e;
-  if (a.dtype == PKD_BF16)
-    e = cudaLaunchKernelEx(&cfg, merge_partials_kernel<__nv_bfloat16>, a.image,
-                           a.partials, out, a.lse, a.num_qo_heads, a.batch,
-                           a.max_partials, a.image_words);
-  else
-    e = cudaLaunchKernelEx(&cfg, merge_partials_kernel<__half>, a.image, a.partials,
-                           out, a.lse, a.num_qo_heads, a.batch, a.max_partials,
-                           a.image_words);
+  cudaError_t e = a.dtype == PKD_BF16 ? launch_merge_typed<__nv_bfloat16>(a, &cfg)
+                                      : launch_merge_typed<__half>(a, &cfg);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

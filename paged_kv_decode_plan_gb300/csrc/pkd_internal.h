@@ -103,6 +103,7 @@ struct MergePartialsArgs {
   void *out;
   float *lse;
   int num_qo_heads, dtype, grid, batch, max_partials, image_words;
+  int num_partials, num_split;  // from the plan, to size the launch
 };
 int launch_merge_partials(const MergePartialsArgs &a, void *stream);
 

@@ -145,7 +145,7 @@ def test_cascade_prefix_suffix_merge():
 
 
 @pytest.mark.parametrize("num_ctas,m", [(1, 1), (7, 1), (152, 1), (300, 1),
-                                        (152, 9), (16, 40)])
+                                        (152, 9), (152, 12), (16, 40), (8, 200)])
 def test_split_geometries(num_ctas, m):
     lengths = [1, 700, 0, 2049, 16, 333, 4096, 17]
     wl = workloads.make_paged("geom", lengths, num_qo_heads=32, num_kv_heads=8,
