@@ -177,6 +177,18 @@ pkd_status pkd_run(const pkd_plan_t *plan, const void *q, const void *k_pages,
                    void *out, float *lse, void *stream);
 
 /*
+ * CUDA graphs ([W] "Plan and run": stable workspace addresses, updated
+ * scheduling data for a captured run).  pkd_run, pkd_run_decode and
+ * pkd_run_merge may be captured on a stream.  While capturing, the merge
+ * kernel is launched even if the plan split nothing, and both launches are
+ * sized for the problem's capacity (max_batch, the float workspace's size),
+ * because they read the plan image at run time: a replay computes whatever
+ * plan pkd_plan last copied into the same int_ws_dev (same problem apart from
+ * batch <= max_batch), with q / out / lse and the page-table buffers at the
+ * captured addresses sized for max_batch and int_ws_dev of pkd_workspace_size.
+ */
+
+/*
  * The two launches of pkd_run, for callers that put other work or events
  * between them: pkd_run_decode launches the decode kernel (same arguments and
  * errors as pkd_run); pkd_run_merge then launches the merge kernel for the

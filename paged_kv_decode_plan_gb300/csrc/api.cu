@@ -16,6 +16,38 @@ pkd_status cuda_fail(cudaError_t e, const char *what) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// True while `stream` is being captured into a CUDA graph.
+bool capturing(void *stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &st) == cudaSuccess &&
+         st == cudaStreamCaptureStatusActive;
+}
+
+// Bounds a launch may trust for the plan image and partial states.  Under
+// capture they are the capacity of the problem and of the float workspace, so
+// that replays stay valid for any later plan of the same problem.
+struct Bounds {
+  int batch, max_partials, image_words;
+};
+
+Bounds launch_bounds(const pkd_plan_t &plan, size_t float_ws_bytes, bool capture) {
+  const pkd_problem &p = plan.problem;
+  Bounds b;
+  const long long slot = pkd::partial_slot_floats(p.num_qo_heads, p.head_dim) * 4;
+  const long long slots = static_cast<long long>(float_ws_bytes) / slot;
+  b.max_partials = static_cast<int>(slots < INT32_MAX ? slots : INT32_MAX);
+  if (capture) {
+    size_t int_ws = 0;
+    pkd::workspace_bytes(p, &int_ws, nullptr, nullptr);
+    b.batch = p.max_batch > 0 ? p.max_batch : p.batch;
+    b.image_words = static_cast<int>(int_ws / 4);
+  } else {
+    b.batch = p.batch;
+    b.image_words = static_cast<int>(plan.int_ws_bytes_used / 4);
+  }
+  return b;
+}
+
 // Fills num_ctas from the current device when it is 0.
 pkd_status resolve_ctas(pkd_problem *p) {
   if (p->num_ctas > 0) return PKD_OK;
@@ -125,15 +157,16 @@ pkd_status pkd_run_decode(const pkd_plan_t *plan, const void *q,
   a.out = out;
   a.lse = lse;
   a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  const Bounds bounds = launch_bounds(*plan, float_ws_bytes, capturing(stream));
   a.num_pages = p.num_pages;
-  a.batch = p.batch;
+  a.batch = bounds.batch;
   a.num_qo_heads = p.num_qo_heads;
   a.num_kv_heads = p.num_kv_heads;
   a.page_size = p.page_size;
   a.num_ctas = p.num_ctas;
   a.dtype = p.dtype;
-  a.max_partials = plan->num_partials;
-  a.image_words = static_cast<int>(plan->int_ws_bytes_used / 4);
+  a.max_partials = bounds.max_partials;
+  a.image_words = bounds.image_words;
   a.loader = p.kv_loader;
   cudaError_t e = static_cast<cudaError_t>(pkd::launch_decode(a, stream));
   if (e == cudaErrorNotSupported)
@@ -150,7 +183,10 @@ pkd_status pkd_run_merge(const pkd_plan_t *plan, const void *int_ws_dev,
   const pkd_problem &p = plan->problem;
   pkd_status st = pkd::check_problem(p, true);
   if (st != PKD_OK) return st;
-  if (plan->num_split_requests == 0) return PKD_OK;
+  // a captured merge runs whatever later plan the image holds, so it is
+  // launched even when this plan split nothing
+  const bool capture = capturing(stream);
+  if (plan->num_split_requests == 0 && !capture) return PKD_OK;
   if (!int_ws_dev || !float_ws_dev || !out || !lse)
     return fail(PKD_ERR_INVALID_ARG, "null device pointer");
   if (!aligned16(out) || !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
@@ -164,11 +200,13 @@ pkd_status pkd_run_merge(const pkd_plan_t *plan, const void *int_ws_dev,
   m.lse = lse;
   m.num_qo_heads = p.num_qo_heads;
   m.dtype = p.dtype;
-  m.batch = p.batch;
-  m.max_partials = plan->num_partials;
-  m.image_words = static_cast<int>(plan->int_ws_bytes_used / 4);
+  const Bounds bounds = launch_bounds(*plan, float_ws_bytes, capture);
+  m.batch = bounds.batch;
+  m.max_partials = bounds.max_partials;
+  m.image_words = bounds.image_words;
   m.num_partials = plan->num_partials;
   m.num_split = plan->num_split_requests;
+  m.rows_bound = capture ? bounds.batch : plan->num_split_requests;
   m.grid = 4 * p.num_ctas;  // upper bound on CTAs; rows loop inside
   cudaError_t e = static_cast<cudaError_t>(pkd::launch_merge_partials(m, stream));
   if (e != cudaSuccess) return cuda_fail(e, "launching the merge kernel");

@@ -95,8 +95,10 @@ struct Params {
   long long num_pages;
   int batch, hq, group, page_size;
   int max_partials;   // partial slots the float workspace holds
-  int image_words;    // int32 words of the plan image
+  int image_words;    // int32 words the image may span
   int grid;           // CTAs launched
+  // batch: requests the q / out / lse / page-table buffers hold; a plan may
+  // cover fewer (a captured launch replayed with a later, smaller plan)
 };
 
 struct Unit {
@@ -542,7 +544,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
   const int num_units = img[kHNumUnits];
   const int num_partials = img[kHNumPartials];
   if (img[kHMagic] != kMagic || img[kHVersion] != kLayoutVersion ||
-      img[kHBatch] != p.batch || img[kHTileTokens] != kTile ||
+      img[kHBatch] < 0 || img[kHBatch] > p.batch || img[kHTileTokens] != kTile ||
       img[kHNumQoHeads] != p.hq || img[kHPageSize] != p.page_size ||
       num_ctas != p.grid || num_units < 0 || num_partials < 0 ||
       num_partials > p.max_partials || img[kHNumSplit] < 0 ||
@@ -553,6 +555,8 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
   const int32_t *cta_ptr = img + kHeaderWords;
   const int32_t *units = cta_ptr + num_ctas + 1;
   const int u_begin = cta_ptr[blockIdx.x], u_end = cta_ptr[blockIdx.x + 1];
+  Params q = p;
+  q.batch = img[kHBatch];  // this plan's batch (p.batch is the buffers' capacity)
   if (u_begin < 0 || u_end > num_units || u_begin > u_end) {
     if (threadIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
     return;
@@ -576,13 +580,13 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
 
   if (threadIdx.x >= 32 * kConsumerWarps) {
     if (LOADER == kLoaderTma)
-      load_tma<HKV>(p, &map_k, &map_v, units, num_partials, u_begin, u_end, stages,
+      load_tma<HKV>(q, &map_k, &map_v, units, num_partials, u_begin, u_end, stages,
                     full0, empty0, abort);
     else
-      load_bulk<HKV>(p, units, num_partials, u_begin, u_end, stages, full0, empty0,
+      load_bulk<HKV>(q, units, num_partials, u_begin, u_end, stages, full0, empty0,
                      abort);
   } else {
-    consume<T, HKV, NG, LOADER>(p, units, num_partials, u_begin, u_end, stages, full0,
+    consume<T, HKV, NG, LOADER>(q, units, num_partials, u_begin, u_end, stages, full0,
                                 empty0, abort);
   }
 }

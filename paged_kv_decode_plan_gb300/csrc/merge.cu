@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   const ImageOffsets o = image_offsets(num_ctas, num_units, num_split);
   // only an image the host planned for this launch is trusted (the decode
   // kernel records a mismatch in the status word)
-  if (image[kHMagic] != kMagic || image[kHBatch] != batch ||
+  if (image[kHMagic] != kMagic || image[kHBatch] < 0 || image[kHBatch] > batch ||
       image[kHNumQoHeads] != hq || num_ctas < 0 || num_units < 0 ||
       num_split < 0 || num_partials < 0 || num_partials > max_partials ||
       o.end > image_words)
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kMergeThreads)
       b = merge_req[i];
       s0 = max(0, merge_indptr[i]);
       s1 = min(num_partials, merge_indptr[i + 1]);
-      if (b < 0 || b >= batch) b = -1;
+      if (b < 0 || b >= image[kHBatch]) b = -1;
     }
     float m = -INFINITY, ws = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(256)
 template <typename T, int WPR>
 cudaError_t launch_merge_wpr(const MergePartialsArgs &a, cudaLaunchConfig_t *cfg) {
   constexpr int kRowsPerCta = kMergeWarps / WPR;
-  const long long rows = static_cast<long long>(a.num_split) * a.num_qo_heads;
+  const long long rows = static_cast<long long>(a.rows_bound) * a.num_qo_heads;
   const long long want = (rows + kRowsPerCta - 1) / kRowsPerCta;
   cfg->gridDim = dim3(static_cast<unsigned>(want < a.grid ? want : a.grid));
   return cudaLaunchKernelEx(cfg, merge_partials_kernel<T, WPR>, a.image, a.partials,

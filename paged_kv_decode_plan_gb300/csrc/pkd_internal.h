@@ -103,7 +103,8 @@ struct MergePartialsArgs {
   void *out;
   float *lse;
   int num_qo_heads, dtype, grid, batch, max_partials, image_words;
-  int num_partials, num_split;  // from the plan, to size the launch
+  int num_partials, num_split;  // from the plan, to choose warps per row
+  int rows_bound;               // split requests the grid is sized for
 };
 int launch_merge_partials(const MergePartialsArgs &a, void *stream);
 

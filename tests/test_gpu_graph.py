@@ -1,0 +1,92 @@
+"""A captured run stays valid for later plans ("FlashInfer"
+(aiwiki.ai/wiki/flashinfer), "Plan and run": stable workspace addresses,
+updated scheduling data passed to a captured run).
+
+One CUDA graph holds the decode and merge launches; between replays the host
+plans a different batch (other lengths, fewer requests, no split at all) into
+the same workspace and rewrites the device page table in place.  Every replay
+must match the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_decode_plan_gb300 as pkd
+from paged_kv_decode_plan_gb300 import workloads
+from tests import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+MAX_BATCH = 6
+POOL = 600
+
+
+def _pool(dtype, seed):
+    """A page pool and queries sized for MAX_BATCH requests."""
+    return workloads.make_paged("graph", [16] * MAX_BATCH, num_qo_heads=32,
+                                num_kv_heads=8, page_size=16, dtype=dtype, seed=seed,
+                                pool_pages=POOL)
+
+
+def _table(lengths, seed):
+    perm = np.random.default_rng(seed).permutation(POOL)
+    return workloads.table_from_lengths(lengths, 16, perm)
+
+
+@pytest.mark.parametrize("dtype,loader", [("f16", pkd.LOADER_AUTO),
+                                          ("bf16", pkd.LOADER_TMA_TILES)])
+def test_captured_run_follows_later_plans(dtype, loader):
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device")
+    base = _pool(dtype, 40)
+    dev = gh.DeviceBatch(base)
+    prob = pkd.make_problem(batch=MAX_BATCH, num_qo_heads=32, num_kv_heads=8,
+                            page_size=16, dtype=dtype, num_pages=POOL, num_ctas=24,
+                            max_batch=MAX_BATCH, kv_loader=loader)
+    ws = pkd.Workspace(prob)
+    # device page table at fixed addresses, sized for the capacity
+    indptr_d = torch.zeros(MAX_BATCH + 1, dtype=torch.int32, device="cuda")
+    indices_d = torch.zeros(POOL, dtype=torch.int32, device="cuda")
+    last_d = torch.zeros(MAX_BATCH, dtype=torch.int32, device="cuda")
+    out = torch.zeros_like(dev.q)
+    lse = torch.zeros(dev.q.shape[:2], dtype=torch.float32, device="cuda")
+
+    def load_table(t):
+        indptr_d.zero_()
+        last_d.zero_()
+        indptr_d[: t.batch + 1].copy_(torch.from_numpy(t.kv_indptr))
+        indices_d[: t.kv_indices.size].copy_(torch.from_numpy(t.kv_indices))
+        last_d[: t.batch].copy_(torch.from_numpy(t.kv_last_page_len))
+
+    first = _table([700, 33, 2000, 5, 1200, 64], 1)
+    load_table(first)
+    plan = ws.plan(first.kv_indptr, first.kv_last_page_len, first.kv_indices)
+    assert plan.num_split_requests > 0
+    # one eager run first (one-time per-device set-up happens outside capture)
+    ws.run(plan, dev.q, dev.k, dev.v, indptr_d, indices_d, last_d, base.sm_scale,
+           out=out, lse=lse)
+    torch.cuda.synchronize()
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ws.run(plan, dev.q, dev.k, dev.v, indptr_d, indices_d, last_d, base.sm_scale,
+               out=out, lse=lse)
+
+    cases = [first,
+             _table([100, 2500, 17, 900, 0, 333], 2),   # other lengths
+             _table([1500, 64, 700], 3),                # fewer requests
+             _table([16, 3, 15, 1, 9, 12], 4)]          # nothing split
+    for t in cases:
+        load_table(t)
+        p = ws.plan(t.kv_indptr, t.kv_last_page_len, t.kv_indices, batch=t.batch)
+        out.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pkd.check_status(ws.int_ws) == 0
+        wl = workloads.PagedBatch("graph", 32, 8, 128, dtype, base.q[: t.batch],
+                                  base.k_pages, base.v_pages, t, base.sm_scale)
+        ref_out, ref_lse = gh.oracle_ref(wl)
+        gh.compare(out[: t.batch], lse[: t.batch], ref_out, ref_lse, dtype)
+        if t is cases[-1]:
+            assert p.num_split_requests == 0
