@@ -45,7 +45,8 @@ DESCRIPTIONS = {
                ">=132 partitions per request",
 }
 KERNEL_SOURCES = ["paged_kv_decode_plan_gb300/csrc/decode.cu",
-                  "paged_kv_decode_plan_gb300/csrc/ptx.cuh"]
+                  "paged_kv_decode_plan_gb300/csrc/ptx.cuh",
+                  "paged_kv_decode_plan_gb300/csrc/kernel_common.cuh"]
 
 
 # ----------------------------------------------------------------- ranks
@@ -215,7 +216,7 @@ class Runner:
     previous step still runs; the decode launch waits only for its own copy.
     """
 
-    def __init__(self, wl, device, kv_loader=0):
+    def __init__(self, wl, device, kv_loader=0, cascade="shared"):
         import torch
         import paged_kv_decode_plan_gb300 as pkd
         self.torch = torch
@@ -225,8 +226,27 @@ class Runner:
         self.q = wl.q.to(device)
         self.k = wl.k_pages.to(device)
         self.v = wl.v_pages.to(device)
-        self.tables = ([wl.extra_tables["prefix"], wl.extra_tables["suffix"]]
-                       if wl.name == "cascade" else [wl.table])
+        # cascade: the shared prefix once through the shared-prefix kernel
+        # ("shared"), or listed in every request's table ("per-request")
+        self.shared = wl.name == "cascade" and cascade == "shared"
+        if wl.name == "cascade" and not self.shared:
+            self.tables = [wl.extra_tables["prefix"], wl.extra_tables["suffix"]]
+        elif self.shared:
+            self.tables = [wl.extra_tables["suffix"]]
+        else:
+            self.tables = [wl.table]
+        self.prefix = None
+        if self.shared:
+            pt = wl.extra_tables["prefix"]
+            pages = pt.kv_indices[: pt.kv_indptr[1]].copy()
+            prob = pkd.make_problem(batch=pt.batch, num_qo_heads=wl.num_qo_heads,
+                                    num_kv_heads=wl.num_kv_heads, page_size=pt.page_size,
+                                    dtype=wl.dtype, num_pages=wl.num_pages)
+            self.prefix = dict(
+                pages=pages, last=int(pt.kv_last_page_len[0]),
+                ws=[pkd.PrefixWorkspace(prob, pages.size, device=device) for _ in range(2)],
+                out=torch.empty_like(self.q),
+                lse=torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
         self.parts = []
         for t in self.tables:
             prob = pkd.make_problem(batch=t.batch, num_qo_heads=wl.num_qo_heads,
@@ -258,10 +278,22 @@ class Runner:
             t = part["table"]
             part["plan"] = part["ws"][i].plan(t.kv_indptr, t.kv_last_page_len, None,
                                               stream=self.copy_stream)
+        if self.prefix is not None:
+            pre = self.prefix
+            pre["plan"] = pre["ws"][i].plan(pre["pages"], pre["last"],
+                                            stream=self.copy_stream)
         ready = torch.cuda.Event()
         ready.record(self.copy_stream)
         main.wait_event(ready)
         launches = 0
+        if self.prefix is not None:
+            if events is not None:
+                events[2].record(main)
+            pre["ws"][i].run(pre["plan"], self.q, self.k, self.v, self.wl.sm_scale,
+                             out=pre["out"], lse=pre["lse"])
+            if events is not None:
+                events[3].record(main)
+            launches += 2
         for n, part in enumerate(self.parts):
             ws, plan = part["ws"][i], part["plan"]
             if events is not None and n == 0:
@@ -273,8 +305,9 @@ class Runner:
             ws.run(plan, self.q, self.k, self.v, *part["dev"], self.wl.sm_scale,
                    out=part["out"], lse=part["lse"], phase="merge")
             launches += 1 + (plan.num_split_requests > 0)
-        if len(self.parts) == 2:
-            a, b = self.parts
+        if len(self.parts) == 2 or self.prefix is not None:
+            a = self.parts[0] if self.prefix is None else self.prefix
+            b = self.parts[-1]
             self.pkd.merge_states(a["out"], a["lse"], b["out"], b["lse"],
                                   v_out=self.final[0], s_out=self.final[1])
             launches += 1
@@ -284,12 +317,15 @@ class Runner:
         self.launches_per_step = launches
 
     def result(self):
-        if len(self.parts) == 2:
+        if len(self.parts) == 2 or self.prefix is not None:
             return self.final
         return self.parts[0]["out"], self.parts[0]["lse"]
 
     def status(self):
-        return max(self.pkd.check_status(ws.int_ws) for p in self.parts for ws in p["ws"])
+        words = [self.pkd.check_status(ws.int_ws) for p in self.parts for ws in p["ws"]]
+        if self.prefix is not None:
+            words += [self.pkd.check_status(ws.int_ws) for ws in self.prefix["ws"]]
+        return max(words)
 
     def kv_bytes(self):
         """Algorithmic KV bytes per step (a shared prefix counted once)."""
@@ -324,7 +360,8 @@ def run_ours(args, ranks):
     torch.cuda.set_device(ranks.local)
     device = torch.device("cuda", ranks.local)
     wl = make_workload(args)
-    runner = Runner(wl, device, kv_loader={"auto": 0, "tma": 1, "bulk": 2}[args.loader])
+    runner = Runner(wl, device, kv_loader={"auto": 0, "tma": 1, "bulk": 2}[args.loader],
+                    cascade=args.cascade)
     stream = torch.cuda.current_stream()
 
     # host plan time (median of 20)
@@ -350,7 +387,7 @@ def run_ours(args, ranks):
     except Exception:  # noqa: BLE001 - older torch
         uuid = None
     k = args.steps
-    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    events = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
               for _ in range(k)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(uuid) as clocks:
@@ -375,7 +412,9 @@ def run_ours(args, ranks):
         # end to end through the public API with host buffers
         e2e = run_e2e(args, runner, device, ranks)
         clocks.mark(1)
-    decode_ms = [a.elapsed_time(b) for a, b in events]
+    decode_ms = [e[0].elapsed_time(e[1]) for e in events]
+    prefix_ms = ([e[2].elapsed_time(e[3]) for e in events]
+                 if runner.prefix is not None else None)
     agg = aggregate(ranks, runner.kv_bytes(), elapsed, k)
     decode_mean_ms = ranks.reduce_max(statistics.fmean(decode_ms))
 
@@ -402,6 +441,9 @@ def run_ours(args, ranks):
         "num_units": runner.parts[0]["plan"].num_units,
         "num_split_requests": runner.parts[0]["plan"].num_split_requests,
         "kv_loader": args.loader,
+        "cascade": (args.cascade if wl.name == "cascade" else None),
+        "prefix_us": (round(statistics.fmean(prefix_ms) * 1e3, 2)
+                      if prefix_ms else None),
         "timing": "pass 1 (value, ms_per_step): K steps between two events; pass 2 "
                   "(decode_us, roofline): the same K steps with events around each "
                   "decode launch",
@@ -575,6 +617,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(DESCRIPTIONS), default="batch64")
     ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--cascade", choices=["shared", "per-request"], default="shared",
+                    help="cascade workload: shared-prefix kernel, or the prefix "
+                         "pages listed in every request's table")
     ap.add_argument("--batch", type=int, default=None,
                     help="smaller batch of the longctx / cascade workload (profiling)")
     ap.add_argument("--loader", choices=["auto", "tma", "bulk"], default="auto",

@@ -260,6 +260,63 @@ pkd_status pkd_run_static(const pkd_plan_t *plan, const int32_t *host_image,
                           const int32_t *kv_last_page_len_d, float sm_scale,
                           void *out, float *lse, void *stream);
 
+/*
+ * Shared-prefix (cascade) attention ([W] "Attention states": a shared prefix
+ * is evaluated separately from request-specific suffixes and the partial
+ * states merged; [D] flashinfer.cascade "Cascade Attention").  The queries of
+ * `problem->batch` requests attend to one KV prefix they all share, stored
+ * once in the page pool as prefix_num_pages pages (all full but the last,
+ * which holds prefix_last_page_len tokens).  out / lse are the states over
+ * the prefix tokens only; pkd_merge_states with the requests' suffix states
+ * (pkd_run on their own pages) gives attention over prefix + suffix.
+ * Per key/value head the prefix work is one dense tile (batch x g query rows
+ * against the prefix), computed once, so the prefix is read once per
+ * (head, 128-row tile, chunk) instead of once per request.
+ * Needs page_size % 16 == 0 (TMA boxes of 16 tokens) and a nonzero
+ * problem->num_ctas-derived chunk count; other fields as for pkd_plan.
+ */
+typedef struct {
+  pkd_problem problem;          /* resolved copy (num_ctas set) */
+  int32_t prefix_len;           /* tokens of the shared prefix */
+  int32_t prefix_num_pages;
+  int32_t chunks;               /* KV chunks of the prefix (partial states per row) */
+  int32_t chunk_tiles;          /* 64-token tiles per chunk */
+  int32_t row_tiles;            /* 128-row tiles per key/value head */
+  int32_t num_blocks;           /* CTAs of the prefix kernel */
+  int64_t int_ws_bytes_used;    /* bytes of the prefix plan image */
+  int64_t float_ws_bytes_needed;/* bytes of fp32 partial states */
+  int32_t valid;
+  int32_t reserved;
+} pkd_prefix_plan_t;
+
+/* Workspace sizes for shared prefixes of up to max_prefix_pages pages. */
+pkd_status pkd_prefix_workspace_size(const pkd_problem *problem,
+                                     int32_t max_prefix_pages,
+                                     size_t *int_ws_bytes, size_t *float_ws_bytes,
+                                     size_t *staging_bytes);
+
+/* Validates the prefix page list on the host (ids in [0, num_pages),
+ * 1 <= last_page_len <= page_size), chooses the chunking, writes the prefix
+ * plan image (header + page ids) into pinned_staging and copies it into
+ * int_ws_dev on `stream`. */
+pkd_status pkd_plan_shared_prefix(const pkd_problem *problem,
+                                  const int32_t *prefix_pages_h,
+                                  int32_t prefix_num_pages,
+                                  int32_t prefix_last_page_len,
+                                  pkd_prefix_plan_t *plan, int32_t *pinned_staging,
+                                  size_t staging_bytes, void *int_ws_dev,
+                                  size_t int_ws_bytes, void *stream);
+
+/* Launches the shared-prefix kernel and the merge of its chunk states.
+ * q [batch][Hq][D], k_pages / v_pages NHD; out [batch][Hq][D], lse [batch][Hq].
+ * Range-check failures and wait timeouts land in the image's status word
+ * (pkd_check_status on int_ws_dev). */
+pkd_status pkd_run_shared_prefix(const pkd_prefix_plan_t *plan, const void *q,
+                                 const void *k_pages, const void *v_pages,
+                                 void *int_ws_dev, void *float_ws_dev,
+                                 size_t float_ws_bytes, float sm_scale, void *out,
+                                 float *lse, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,8 @@ STATUS_NAMES = {0: "PKD_OK", -1: "PKD_ERR_INVALID_ARG", -2: "PKD_ERR_PAGE_TABLE"
 EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
             "pkd_plan_host", "pkd_plan", "pkd_run", "pkd_run_decode",
             "pkd_run_merge", "pkd_merge_states", "pkd_check_status",
-            "pkd_run_static")
+            "pkd_run_static", "pkd_prefix_workspace_size", "pkd_plan_shared_prefix",
+            "pkd_run_shared_prefix")
 
 
 class PkdError(RuntimeError):
@@ -59,6 +60,15 @@ class Plan(ctypes.Structure):
                 ("int_ws_bytes_used", ctypes.c_int64),
                 ("float_ws_bytes_needed", ctypes.c_int64),
                 ("valid", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class PrefixPlan(ctypes.Structure):
+    _fields_ = [("problem", Problem), ("prefix_len", ctypes.c_int32),
+                ("prefix_num_pages", ctypes.c_int32), ("chunks", ctypes.c_int32),
+                ("chunk_tiles", ctypes.c_int32), ("row_tiles", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("int_ws_bytes_used", ctypes.c_int64),
+                ("float_ws_bytes_needed", ctypes.c_int64), ("valid", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -93,9 +103,17 @@ def load():
     lib.pkd_check_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.pkd_run_static.argtypes = [ctypes.POINTER(Plan), i32p, vp, vp, vp, vp, vp,
                                    vp, ctypes.c_float, vp, vp, vp]
+    lib.pkd_prefix_workspace_size.argtypes = [ctypes.POINTER(Problem), ctypes.c_int32,
+                                              sz, sz, sz]
+    lib.pkd_plan_shared_prefix.argtypes = [ctypes.POINTER(Problem), i32p, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.POINTER(PrefixPlan),
+                                           vp, ctypes.c_size_t, vp, ctypes.c_size_t, vp]
+    lib.pkd_run_shared_prefix.argtypes = [ctypes.POINTER(PrefixPlan), vp, vp, vp, vp, vp,
+                                          ctypes.c_size_t, ctypes.c_float, vp, vp, vp]
     for name in ("pkd_workspace_size", "pkd_plan_host", "pkd_plan", "pkd_run",
                  "pkd_run_decode", "pkd_run_merge", "pkd_merge_states",
-                 "pkd_check_status", "pkd_run_static"):
+                 "pkd_check_status", "pkd_run_static", "pkd_prefix_workspace_size",
+                 "pkd_plan_shared_prefix", "pkd_run_shared_prefix"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.pkd_abi_version() != 2:
         raise RuntimeError("libpkd.so ABI version mismatch")
@@ -285,6 +303,81 @@ def check_status(int_ws, stream=None) -> int:
     if st not in (0, -6):
         _check(st)
     return int(word.value)
+
+
+def prefix_workspace_size(problem: Problem, max_prefix_pages: int):
+    """(int_ws_bytes, float_ws_bytes, staging_bytes) for shared prefixes."""
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().pkd_prefix_workspace_size(ctypes.byref(problem), int(max_prefix_pages),
+                                            ctypes.byref(a), ctypes.byref(b),
+                                            ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def plan_shared_prefix(problem: Problem, prefix_pages, prefix_last_page_len, *,
+                       staging, int_ws, stream=None) -> PrefixPlan:
+    """Plans attention of ``problem.batch`` requests against one shared prefix."""
+    pages, p_pages = _host_i32(prefix_pages)
+    n = 0 if prefix_pages is None else int(np.asarray(prefix_pages).size)
+    out = PrefixPlan()
+    _check(load().pkd_plan_shared_prefix(
+        ctypes.byref(problem), p_pages, n, int(prefix_last_page_len), ctypes.byref(out),
+        _ptr(staging), staging.numel() * staging.element_size(), _ptr(int_ws),
+        int_ws.numel() * int_ws.element_size(), _stream_ptr(stream)))
+    return out
+
+
+def run_shared_prefix(plan_: PrefixPlan, q, k_pages, v_pages, int_ws, float_ws,
+                      sm_scale: float, out=None, lse=None, stream=None):
+    """States of every (request, query head) over the shared prefix."""
+    import torch
+    p = plan_.problem
+    if out is None:
+        out = torch.empty((p.batch, p.num_qo_heads, p.head_dim), dtype=q.dtype,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((p.batch, p.num_qo_heads), dtype=torch.float32,
+                          device=q.device)
+    if _dtype_code(q.dtype) != p.dtype or k_pages.dtype != q.dtype or \
+            v_pages.dtype != q.dtype or out.dtype != q.dtype:
+        raise ValueError("dtype does not match the plan")
+    _check(load().pkd_run_shared_prefix(
+        ctypes.byref(plan_), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(int_ws),
+        _ptr(float_ws), float_ws.numel() * float_ws.element_size(), float(sm_scale),
+        _ptr(out), _ptr(lse), _stream_ptr(stream)))
+    return out, lse
+
+
+class PrefixWorkspace:
+    """Workspaces and pinned staging for shared prefixes of a capacity."""
+
+    def __init__(self, problem: Problem, max_prefix_pages: int, device=None):
+        import torch
+        self.problem = Problem.from_buffer_copy(problem)
+        ib, fb, sb = prefix_workspace_size(self.problem, max_prefix_pages)
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        self.int_ws = torch.zeros(ib, dtype=torch.uint8, device=device)
+        self.float_ws = torch.empty(max(fb, 16), dtype=torch.uint8, device=device)
+        self.staging = torch.empty(sb // 4 + 4, dtype=torch.int32, pin_memory=True)
+        self.event = None
+
+    def plan(self, prefix_pages, prefix_last_page_len, *, batch=None, stream=None):
+        import torch
+        prob = Problem.from_buffer_copy(self.problem)
+        if batch is not None:
+            prob.batch = batch
+        if self.event is not None:
+            self.event.synchronize()
+        out = plan_shared_prefix(prob, prefix_pages, prefix_last_page_len,
+                                 staging=self.staging, int_ws=self.int_ws, stream=stream)
+        self.event = torch.cuda.Event()
+        self.event.record(stream or torch.cuda.current_stream())
+        return out
+
+    def run(self, plan_: PrefixPlan, q, k_pages, v_pages, sm_scale, out=None, lse=None,
+            stream=None):
+        return run_shared_prefix(plan_, q, k_pages, v_pages, self.int_ws, self.float_ws,
+                                 sm_scale, out=out, lse=lse, stream=stream)
 
 
 class Workspace:

@@ -20,8 +20,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build", platform.machine())
 LIB_PATH = os.path.join(HERE, "libpkd.so")
 
-SOURCES = ["plan.cpp", "api.cu", "decode.cu", "merge.cu", "static_scratch.cu"]
-HEADERS = ["pkd_internal.h", "ptx.cuh"]
+SOURCES = ["plan.cpp", "api.cu", "decode.cu", "merge.cu", "prefix.cu",
+           "static_scratch.cu"]
+HEADERS = ["pkd_internal.h", "ptx.cuh", "kernel_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
           "-I" + INCLUDE, "-I" + CSRC]

@@ -250,6 +250,100 @@ pkd_status pkd_merge_states(const void *v_a, const float *s_a, const void *v_b,
   return PKD_OK;
 }
 
+pkd_status pkd_prefix_workspace_size(const pkd_problem *problem,
+                                     int32_t max_prefix_pages, size_t *int_ws_bytes,
+                                     size_t *float_ws_bytes, size_t *staging_bytes) {
+  pkd::clear_error();
+  if (!problem) return fail(PKD_ERR_INVALID_ARG, "null problem");
+  if (max_prefix_pages < 0) return fail(PKD_ERR_INVALID_ARG, "negative page count");
+  pkd_problem p = *problem;
+  pkd_status st = resolve_ctas(&p);
+  if (st != PKD_OK) return st;
+  st = pkd::check_problem(p, true);
+  if (st != PKD_OK) return st;
+  pkd::prefix_workspace_bytes(p, max_prefix_pages, int_ws_bytes, float_ws_bytes,
+                              staging_bytes);
+  return PKD_OK;
+}
+
+pkd_status pkd_plan_shared_prefix(const pkd_problem *problem,
+                                  const int32_t *prefix_pages_h,
+                                  int32_t prefix_num_pages,
+                                  int32_t prefix_last_page_len,
+                                  pkd_prefix_plan_t *plan, int32_t *pinned_staging,
+                                  size_t staging_bytes, void *int_ws_dev,
+                                  size_t int_ws_bytes, void *stream) {
+  pkd::clear_error();
+  if (!problem || !int_ws_dev) return fail(PKD_ERR_INVALID_ARG, "null pointer");
+  pkd_problem p = *problem;
+  pkd_status st = resolve_ctas(&p);
+  if (st != PKD_OK) return st;
+  st = pkd::plan_prefix_impl(p, prefix_pages_h, prefix_num_pages, prefix_last_page_len,
+                             plan, pinned_staging, staging_bytes);
+  if (st != PKD_OK) return st;
+  if (static_cast<size_t>(plan->int_ws_bytes_used) > int_ws_bytes) {
+    plan->valid = 0;
+    return fail(PKD_ERR_WORKSPACE, "int workspace smaller than the prefix plan image");
+  }
+  cudaError_t e = cudaMemcpyAsync(int_ws_dev, pinned_staging,
+                                  static_cast<size_t>(plan->int_ws_bytes_used),
+                                  cudaMemcpyHostToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    plan->valid = 0;
+    return cuda_fail(e, "copying the prefix plan image");
+  }
+  return PKD_OK;
+}
+
+pkd_status pkd_run_shared_prefix(const pkd_prefix_plan_t *plan, const void *q,
+                                 const void *k_pages, const void *v_pages,
+                                 void *int_ws_dev, void *float_ws_dev,
+                                 size_t float_ws_bytes, float sm_scale, void *out,
+                                 float *lse, void *stream) {
+  pkd::clear_error();
+  if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "plan not valid");
+  const pkd_problem &p = plan->problem;
+  pkd_status st = pkd::check_problem(p, true);
+  if (st != PKD_OK) return st;
+  if (p.batch == 0) return PKD_OK;
+  if (!q || !k_pages || !v_pages || !int_ws_dev || !float_ws_dev || !out || !lse)
+    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
+      !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
+    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
+  if (float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed))
+    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the prefix plan needs");
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f))
+    return fail(PKD_ERR_INVALID_ARG, "sm_scale must be finite and positive");
+  pkd::PrefixArgs a;
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.image = static_cast<int32_t *>(int_ws_dev);
+  a.partials = static_cast<float *>(float_ws_dev);
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.num_pages = p.num_pages;
+  a.batch = p.batch;
+  a.num_qo_heads = p.num_qo_heads;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  a.dtype = p.dtype;
+  a.length = plan->prefix_len;
+  a.chunks = plan->chunks;
+  a.chunk_tiles = plan->chunk_tiles;
+  a.row_tiles = plan->row_tiles;
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_shared_prefix(a, stream));
+  if (e == cudaErrorNotSupported)
+    return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");
+  if (e != cudaSuccess) return cuda_fail(e, "launching the shared-prefix kernel");
+  e = static_cast<cudaError_t>(pkd::launch_merge_uniform(
+      static_cast<const float *>(float_ws_dev), out, lse, p.batch, p.num_qo_heads,
+      plan->chunks, p.dtype, 4 * p.num_ctas, stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the prefix merge");
+  return PKD_OK;
+}
+
 pkd_status pkd_check_status(const void *int_ws_dev, uint32_t *device_status,
                             void *stream) {
   pkd::clear_error();

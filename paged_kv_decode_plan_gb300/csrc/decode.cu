@@ -47,6 +47,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "kernel_common.cuh"
 #include "pkd_internal.h"
 #include "ptx.cuh"
 
@@ -54,13 +55,7 @@ namespace pkd {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kTile = 16;                           // tokens per tile
-constexpr int kRowBytes = kHeadDim * 2;             // one token, one head
-constexpr int kHalfBytes = kTile * 128;             // 16 rows x 64 elements
 constexpr int kStageBudget = 200 * 1024;            // bytes of stages per CTA
-constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kLazy = 8.f;                        // log2 of the largest p
-constexpr long long kWaitPolls = 1ll << 22;         // bounded mbarrier waits
 
 enum Loader : int { kLoaderTma = PKD_LOADER_TMA_TILES, kLoaderBulk = PKD_LOADER_BULK_ROWS };
 
@@ -105,10 +100,6 @@ struct Unit {
   int req, t0, t1, slot, pbase;
 };
 
-__device__ __forceinline__ void flag(int32_t *image, unsigned bit) {
-  atomicOr(reinterpret_cast<unsigned int *>(image + kHStatus), bit);
-}
-
 // Reads unit u and checks it against the device page table.  Every thread
 // computes the same result; a unit that fails is reduced to an empty range
 // (and, if its request id is invalid, to req = -1: nothing is written).
@@ -148,27 +139,9 @@ __device__ __forceinline__ int unit_tiles(const Unit &u) {
   return (u.t1 - u.t0 + kTile - 1) / kTile;
 }
 
-// Polls an mbarrier phase; gives up (false) after kWaitPolls polls or once
-// another warp has given up.  `patient` waits ignore the abort flag.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
-                                           volatile int *abort, bool patient = false) {
-  for (long long i = 0; i < kWaitPolls; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (!patient && (i & 63) == 63 && *abort) return false;
-  }
-  return false;
-}
-
 __device__ __forceinline__ void give_up(const Params &p, volatile int *abort) {
   *abort = 1;
   flag(p.image, PKD_DEVICE_TIMEOUT);
-}
-
-// Byte offset of 16-byte chunk c (0..15) of token row r (0..15) within one
-// head's K or V tile: [d-half][row][128 B], chunks XOR-swizzled by row as the
-// TMA 128-byte swizzle lays them out.
-__device__ __forceinline__ uint32_t tile_offset(int r, int c) {
-  return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
 // Offset of chunk c of token row r of head h within a stage's K (or V) tile.
@@ -641,6 +614,9 @@ int launch_heads(const Params &prm, int hkv, int loader, const CUtensorMap &mk,
   }
 }
 
+}  // namespace
+
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -675,7 +651,8 @@ bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
 
 // Tensor maps of the last page pools seen (encoding is pure host work, but a
 // serving loop passes the same pools on every step).
-bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const DecodeArgs &a) {
+bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
+                 long long num_pages, int page_size, int hkv) {
   struct Entry {
     const void *k, *v;
     long long num_pages;
@@ -688,23 +665,23 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const DecodeArgs &a) {
   static int next = 0;
   std::lock_guard<std::mutex> lock(mutex);
   for (const Entry &e : cache)
-    if (e.k == a.k_pages && e.v == a.v_pages && e.num_pages == a.num_pages &&
-        e.page_size == a.page_size && e.hkv == a.num_kv_heads && e.k) {
+    if (e.k == k && e.v == v && e.num_pages == num_pages && e.page_size == page_size &&
+        e.hkv == hkv && e.k) {
       *mk = e.mk;
       *mv = e.mv;
       return true;
     }
   Entry &e = cache[next];
-  if (!encode_pages(&e.mk, a.k_pages, a.num_pages, a.page_size, a.num_kv_heads) ||
-      !encode_pages(&e.mv, a.v_pages, a.num_pages, a.page_size, a.num_kv_heads)) {
+  if (!encode_pages(&e.mk, k, num_pages, page_size, hkv) ||
+      !encode_pages(&e.mv, v, num_pages, page_size, hkv)) {
     e.k = nullptr;
     return false;
   }
-  e.k = a.k_pages;
-  e.v = a.v_pages;
-  e.num_pages = a.num_pages;
-  e.page_size = a.page_size;
-  e.hkv = a.num_kv_heads;
+  e.k = k;
+  e.v = v;
+  e.num_pages = num_pages;
+  e.page_size = page_size;
+  e.hkv = hkv;
   next = (next + 1) % 8;
   *mk = e.mk;
   *mv = e.mv;
@@ -712,6 +689,11 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const DecodeArgs &a) {
 }
 
 }  // namespace
+
+bool page_tensor_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
+                      long long num_pages, int page_size, int hkv) {
+  return cached_maps(mk, mv, k, v, num_pages, page_size, hkv);
+}
 
 int launch_decode(const DecodeArgs &a, void *stream) {
   Params prm;
@@ -745,7 +727,8 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   if (a.loader == PKD_LOADER_TMA_TILES) {
     if (a.page_size % kTile != 0 || a.num_pages <= 0 ||
         a.num_pages * static_cast<long long>(a.page_size) >= (1ll << 31) ||
-        !cached_maps(&mk, &mv, a))
+        !cached_maps(&mk, &mv, a.k_pages, a.v_pages, a.num_pages, a.page_size,
+                     a.num_kv_heads))
       return cudaErrorNotSupported;
     loader = kLoaderTma;
   }

@@ -21,6 +21,84 @@ namespace {
 constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = 32 * kMergeWarps;
 
+// Folds partial states s0, s0 + stride, ... (< s1) of query head h into a
+// running (m, ws, acc) by the online rule: a new maximum rescales what was
+// folded so far; four states' loads are in flight per step.
+__device__ __forceinline__ void fold_states(const float *partials, long long slot_floats,
+                                            int hq, int h, int s0, int s1, int stride,
+                                            int lane, float &m, float &ws, float4 &acc) {
+  constexpr int kUnroll = 4;
+  for (int j = s0; j < s1; j += kUnroll * stride) {
+    float sv[kUnroll];
+    float4 ov[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      const int jj = j + k * stride;
+      sv[k] = -INFINITY;
+      ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (jj < s1) {
+        const float *base = partials + jj * slot_floats;
+        sv[k] = base[hq * kHeadDim + h];
+        ov[k] = reinterpret_cast<const float4 *>(base + h * kHeadDim)[lane];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      if (sv[k] > m) {
+        const float f = m == -INFINITY ? 0.f : expf(m - sv[k]);
+        acc.x *= f;
+        acc.y *= f;
+        acc.z *= f;
+        acc.w *= f;
+        ws *= f;
+        m = sv[k];
+      }
+      const float w = sv[k] == -INFINITY ? 0.f : expf(sv[k] - m);
+      acc.x += w * ov[k].x;
+      acc.y += w * ov[k].y;
+      acc.z += w * ov[k].z;
+      acc.w += w * ov[k].w;
+      ws += w;
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void write_state(uint16_t *out, float *lse, int b, int hq,
+                                            int h, int lane, float m, float ws,
+                                            float4 acc) {
+  const float inv = ws > 0.f ? 1.f / ws : 0.f;
+  uint16_t *dst = out + (static_cast<long long>(b) * hq + h) * kHeadDim + 4 * lane;
+  uint2 packed;
+  packed.x = ptx::pack2<T>(acc.x * inv, acc.y * inv);
+  packed.y = ptx::pack2<T>(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2 *>(dst) = packed;
+  if (lane == 0)
+    lse[static_cast<long long>(b) * hq + h] = ws > 0.f ? m + logf(ws) : -INFINITY;
+}
+
+// Chunk merge of the shared-prefix kernel: every request has `chunks` partial
+// states in slots b * chunks .. b * chunks + chunks - 1; one warp per
+// (request, head) row.
+template <typename T>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_uniform_kernel(const float *partials, uint16_t *out, float *lse, int batch,
+                         int hq, int chunks) {
+  const int lane = threadIdx.x & 31;
+  const long long slot_floats = partial_slot_floats(hq, kHeadDim);
+  const long long rows = static_cast<long long>(batch) * hq;
+  ptx::wait_primary_grid();
+  for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       row < rows; row += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    const int b = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
+    float m = -INFINITY, ws = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    fold_states(partials, slot_floats, hq, h, b * chunks, (b + 1) * chunks, 1, lane, m,
+                ws, acc);
+    write_state<T>(out, lse, b, hq, h, lane, m, ws, acc);
+  }
+}
+
 // Split-KV merge.  A (split request, query head) row is handled by WPR warps
 // (1, 2, 4 or 8, chosen from the average number of partial states per split
 // request); each warp folds its share of the row's partial states in one
@@ -33,7 +111,6 @@ __global__ void __launch_bounds__(kMergeThreads)
                           uint16_t *out, float *lse, int hq, int batch,
                           int max_partials, int image_words) {
   constexpr int kRowsPerCta = kMergeWarps / WPR;
-  constexpr int kUnroll = 4;
   __shared__ float4 red_acc[kMergeWarps][32];
   __shared__ float red_w[kMergeWarps];
   __shared__ float red_m[kMergeWarps];
@@ -74,41 +151,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
     float m = -INFINITY, ws = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (b >= 0) {
-      for (int j = s0 + sub; j < s1; j += kUnroll * WPR) {
-        float sv[kUnroll];
-        float4 ov[kUnroll];
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-          const int jj = j + k * WPR;
-          sv[k] = -INFINITY;
-          ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (jj < s1) {
-            const float *base = partials + jj * slot_floats;
-            sv[k] = base[hq * kHeadDim + h];
-            ov[k] = reinterpret_cast<const float4 *>(base + h * kHeadDim)[lane];
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-          if (sv[k] > m) {  // new maximum: rescale what was folded so far
-            const float f = m == -INFINITY ? 0.f : expf(m - sv[k]);
-            acc.x *= f;
-            acc.y *= f;
-            acc.z *= f;
-            acc.w *= f;
-            ws *= f;
-            m = sv[k];
-          }
-          const float w = sv[k] == -INFINITY ? 0.f : expf(sv[k] - m);
-          acc.x += w * ov[k].x;
-          acc.y += w * ov[k].y;
-          acc.z += w * ov[k].z;
-          acc.w += w * ov[k].w;
-          ws += w;
-        }
-      }
-    }
+    if (b >= 0)
+      fold_states(partials, slot_floats, hq, h, s0 + sub, s1, WPR, lane, m, ws, acc);
     if (WPR > 1) {
       red_acc[warp][lane] = acc;
       if (lane == 0) {
@@ -140,16 +184,7 @@ __global__ void __launch_bounds__(kMergeThreads)
         m = mm;
       }
     }
-    if (sub == 0 && b >= 0) {
-      const float inv = ws > 0.f ? 1.f / ws : 0.f;
-      uint16_t *dst = out + (static_cast<long long>(b) * hq + h) * kHeadDim + 4 * lane;
-      uint2 packed;
-      packed.x = ptx::pack2<T>(acc.x * inv, acc.y * inv);
-      packed.y = ptx::pack2<T>(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2 *>(dst) = packed;
-      if (lane == 0)
-        lse[static_cast<long long>(b) * hq + h] = ws > 0.f ? m + logf(ws) : -INFINITY;
-    }
+    if (sub == 0 && b >= 0) write_state<T>(out, lse, b, hq, h, lane, m, ws, acc);
     if (WPR > 1) __syncthreads();
   }
 }
@@ -271,6 +306,30 @@ int launch_merge_partials(const MergePartialsArgs &a, void *stream) {
   cfg.numAttrs = 1;
   cudaError_t e = a.dtype == PKD_BF16 ? launch_merge_typed<__nv_bfloat16>(a, &cfg)
                                       : launch_merge_typed<__half>(a, &cfg);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+int launch_merge_uniform(const float *partials, void *out, float *lse, int batch, int hq,
+                         int chunks, int dtype, int grid, void *stream) {
+  const long long rows = static_cast<long long>(batch) * hq;
+  if (rows == 0) return cudaSuccess;
+  const long long want = (rows + kMergeWarps - 1) / kMergeWarps;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < grid ? want : grid));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  uint16_t *o = static_cast<uint16_t *>(out);
+  cudaError_t e = dtype == PKD_BF16
+                      ? cudaLaunchKernelEx(&cfg, merge_uniform_kernel<__nv_bfloat16>,
+                                           partials, o, lse, batch, hq, chunks)
+                      : cudaLaunchKernelEx(&cfg, merge_uniform_kernel<__half>, partials,
+                                           o, lse, batch, hq, chunks);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -108,6 +108,40 @@ struct MergePartialsArgs {
 };
 int launch_merge_partials(const MergePartialsArgs &a, void *stream);
 
+// Shared-prefix attention (prefix.cu) and its chunk merge (merge.cu).
+constexpr int kPrefixMagic = 0x50444B50;  // "PKDP"
+enum PrefixHeaderWord {
+  kPBatch = 2, kPNumQoHeads = 3, kPNumKvHeads = 4, kPPageSize = 5, kPLength = 6,
+  kPNumPages = 7, kPChunks = 8, kPChunkTiles = 9, kPRowTiles = 10,
+};
+struct PrefixArgs {
+  const void *q, *k_pages, *v_pages;
+  int32_t *image;
+  float *partials;
+  float sm_scale_log2;
+  int64_t num_pages;
+  int batch, num_qo_heads, num_kv_heads, page_size, dtype;
+  int length, chunks, chunk_tiles, row_tiles;
+};
+int launch_shared_prefix(const PrefixArgs &a, void *stream);
+int prefix_tile_tokens();
+int prefix_tile_rows();
+int launch_merge_uniform(const float *partials, void *out, float *lse, int batch, int hq,
+                         int chunks, int dtype, int grid, void *stream);
+pkd_status plan_prefix_impl(const pkd_problem &in, const int32_t *pages,
+                            int32_t num_prefix_pages, int32_t last_page_len,
+                            pkd_prefix_plan_t *plan, int32_t *image, size_t image_bytes);
+void prefix_workspace_bytes(const pkd_problem &p, int32_t max_prefix_pages,
+                            size_t *int_ws, size_t *float_ws, size_t *staging);
+
+// Tensor maps for K and V page pools viewed as [token row][head][d]: boxes of
+// 16 token rows x 1 head x 64 elements, 128-byte swizzle; cached per pool.
+// (CUtensorMap comes from <cuda.h>; callers include it first.)
+#ifdef CUDA_VERSION
+bool page_tensor_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
+                      long long num_pages, int page_size, int hkv);
+#endif
+
 int launch_merge_states(const void *v_a, const float *s_a, const void *v_b,
                         const float *s_b, void *v_out, float *s_out, int64_t n,
                         int num_heads, int head_dim, int dtype, void *stream);

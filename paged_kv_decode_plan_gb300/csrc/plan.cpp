@@ -243,4 +243,93 @@ pkd_status plan_host_impl(const pkd_problem &in, const int32_t *kv_indptr,
   return PKD_OK;
 }
 
+// Shared-prefix planning: validate the page list, split the prefix into KV
+// chunks so that (heads x row tiles x chunks) fills the CTA budget, write the
+// image (header + page ids).
+namespace {
+constexpr int kPrefixTile = 64;   // tokens per prefix stage (prefix.cu)
+constexpr int kPrefixRows = 128;  // query rows per prefix CTA (prefix.cu)
+}  // namespace
+
+void prefix_workspace_bytes(const pkd_problem &p, int32_t max_prefix_pages,
+                            size_t *int_ws, size_t *float_ws, size_t *staging) {
+  const int64_t cap_batch = p.max_batch > 0 ? p.max_batch : p.batch;
+  const int64_t max_chunks = std::max(1, p.num_ctas / std::max(1, p.num_kv_heads));
+  const size_t ib = static_cast<size_t>(kHeaderWords + std::max(0, max_prefix_pages)) * 4;
+  if (int_ws) *int_ws = ib;
+  if (staging) *staging = ib;
+  if (float_ws)
+    *float_ws = static_cast<size_t>(cap_batch * max_chunks) *
+                partial_slot_floats(p.num_qo_heads, p.head_dim) * sizeof(float);
+}
+
+pkd_status plan_prefix_impl(const pkd_problem &in, const int32_t *pages,
+                            int32_t num_prefix_pages, int32_t last_page_len,
+                            pkd_prefix_plan_t *plan, int32_t *image, size_t image_bytes) {
+  if (!plan || !image || (num_prefix_pages > 0 && !pages))
+    return fail(PKD_ERR_INVALID_ARG, "null pointer");
+  pkd_problem p = in;
+  if (p.tile_tokens == 0) p.tile_tokens = kTileTokens;
+  pkd_status st = check_problem(p, true);
+  if (st != PKD_OK) return st;
+  if (p.page_size % kTileTokens != 0)
+    return fail(PKD_ERR_UNSUPPORTED, "shared prefix needs page_size % 16 == 0");
+  if (num_prefix_pages < 0) return fail(PKD_ERR_INVALID_ARG, "negative page count");
+  if (num_prefix_pages > 0 && (last_page_len < 1 || last_page_len > p.page_size))
+    return fail(PKD_ERR_PAGE_TABLE, "prefix last_page_len out of [1, page_size]");
+  for (int32_t i = 0; i < num_prefix_pages; ++i)
+    if (pages[i] < 0 || pages[i] >= p.num_pages)
+      return fail(PKD_ERR_PAGE_TABLE,
+                  "prefix page id out of range at index " + std::to_string(i));
+  const int64_t length =
+      num_prefix_pages > 0
+          ? static_cast<int64_t>(num_prefix_pages - 1) * p.page_size + last_page_len
+          : 0;
+  if (length > INT32_MAX - kPrefixTile ||
+      static_cast<int64_t>(p.num_pages) * p.page_size >= (1ll << 31))
+    return fail(PKD_ERR_UNSUPPORTED, "prefix or pool too long for 32-bit token rows");
+  const int64_t need = static_cast<int64_t>(kHeaderWords + num_prefix_pages) * 4;
+  if (static_cast<size_t>(need) > image_bytes)
+    return fail(PKD_ERR_WORKSPACE, "prefix plan image needs " + std::to_string(need) +
+                                       " bytes, buffer has " + std::to_string(image_bytes));
+  const int group = p.num_qo_heads / p.num_kv_heads;
+  const int64_t rows = static_cast<int64_t>(p.batch) * group;
+  const int row_tiles = static_cast<int>(std::max<int64_t>(1, (rows + kPrefixRows - 1) / kPrefixRows));
+  const int total_tiles = static_cast<int>((length + kPrefixTile - 1) / kPrefixTile);
+  const int base = p.num_kv_heads * row_tiles;
+  int chunks = std::max(1, std::min(total_tiles, p.num_ctas / base));
+  int chunk_tiles = total_tiles > 0 ? (total_tiles + chunks - 1) / chunks : 0;
+  if (chunk_tiles > 0) chunks = (total_tiles + chunk_tiles - 1) / chunk_tiles;
+
+  std::memset(image, 0, kHeaderWords * sizeof(int32_t));
+  image[kHMagic] = kPrefixMagic;
+  image[kHVersion] = 1;
+  image[kPBatch] = p.batch;
+  image[kPNumQoHeads] = p.num_qo_heads;
+  image[kPNumKvHeads] = p.num_kv_heads;
+  image[kPPageSize] = p.page_size;
+  image[kPLength] = static_cast<int32_t>(length);
+  image[kPNumPages] = num_prefix_pages;
+  image[kPChunks] = chunks;
+  image[kPChunkTiles] = chunk_tiles;
+  image[kPRowTiles] = row_tiles;
+  image[kHStatus] = 0;
+  if (num_prefix_pages > 0)
+    std::memcpy(image + kHeaderWords, pages, num_prefix_pages * sizeof(int32_t));
+
+  std::memset(plan, 0, sizeof(*plan));
+  plan->problem = p;
+  plan->prefix_len = static_cast<int32_t>(length);
+  plan->prefix_num_pages = num_prefix_pages;
+  plan->chunks = chunks;
+  plan->chunk_tiles = chunk_tiles;
+  plan->row_tiles = row_tiles;
+  plan->num_blocks = p.num_kv_heads * row_tiles * chunks;
+  plan->int_ws_bytes_used = need;
+  plan->float_ws_bytes_needed = static_cast<int64_t>(p.batch) * chunks *
+                                partial_slot_floats(p.num_qo_heads, p.head_dim) * 4;
+  plan->valid = 1;
+  return PKD_OK;
+}
+
 }  // namespace pkd

@@ -1,0 +1,109 @@
+"""Shared-prefix (cascade) attention against the oracle.
+
+"FlashInfer" (aiwiki.ai/wiki/flashinfer), "Attention states": a shared prefix
+evaluated separately from the request-specific suffixes, then merged.  The
+prefix kernel's states must equal attention over a table in which every
+request lists the prefix pages; prefix states merged with suffix states must
+equal attention over prefix + suffix.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_decode_plan_gb300 as pkd
+from paged_kv_decode_plan_gb300 import workloads
+from tests import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefix_case(batch, hq, hkv, page, length, dtype, seed):
+    npages = (length + page - 1) // page
+    pool = max(npages, batch) + 5
+    wl = workloads.make_paged("prefix", [16] * batch, num_qo_heads=hq, num_kv_heads=hkv,
+                              page_size=page, dtype=dtype, seed=seed, pool_pages=pool)
+    pages = np.random.default_rng(seed).permutation(pool)[:npages].astype(np.int32)
+    last = length - (npages - 1) * page if npages else 0
+    table = workloads.PageTable(
+        (np.arange(batch + 1) * npages).astype(np.int32),
+        np.tile(pages, batch).astype(np.int32),
+        np.full(batch, last, dtype=np.int32), page)
+    return wl, pages, last, table
+
+
+def _run_prefix(dev, wl, pages, last, num_ctas=0):
+    prob = pkd.make_problem(batch=wl.batch, num_qo_heads=wl.num_qo_heads,
+                            num_kv_heads=wl.num_kv_heads, page_size=wl.page_size,
+                            dtype=wl.dtype, num_pages=wl.num_pages, num_ctas=num_ctas)
+    pws = pkd.PrefixWorkspace(prob, max(1, pages.size))
+    plan = pws.plan(pages, last)
+    out, lse = pws.run(plan, dev.q, dev.k, dev.v, wl.sm_scale)
+    torch.cuda.synchronize()
+    return out, lse, plan, pkd.check_status(pws.int_ws)
+
+
+CASES = [
+    # batch, hq, hkv, page, prefix length, dtype, num_ctas
+    (1, 32, 8, 16, 512, "f16", 0),
+    (3, 32, 8, 16, 17, "bf16", 0),
+    (40, 32, 8, 16, 3000, "f16", 0),
+    (40, 32, 8, 16, 3000, "bf16", 7),
+    (5, 64, 8, 64, 1000, "bf16", 0),
+    (9, 8, 8, 32, 65, "f16", 152),
+    (2, 16, 1, 16, 2049, "bf16", 3),
+    (70, 32, 4, 16, 640, "f16", 0),
+    (4, 32, 8, 16, 1, "f16", 0),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_shared_prefix_matches_oracle(case):
+    batch, hq, hkv, page, length, dtype, ctas = case
+    wl, pages, last, table = _prefix_case(batch, hq, hkv, page, length, dtype,
+                                          seed=batch * 7 + length)
+    dev = gh.DeviceBatch(wl)
+    out, lse, plan, status = _run_prefix(dev, wl, pages, last, ctas)
+    assert status == 0
+    assert plan.prefix_len == length and plan.chunks >= 1
+    ref_out, ref_lse = gh.oracle_ref(wl, table=table)
+    gh.compare(out, lse, ref_out, ref_lse, dtype)
+
+
+def test_shared_prefix_rejects_bad_pages_and_page_sizes():
+    wl, pages, last, _ = _prefix_case(2, 32, 8, 16, 100, "f16", 1)
+    prob = pkd.make_problem(batch=2, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                            dtype="f16", num_pages=wl.num_pages, num_ctas=8)
+    pws = pkd.PrefixWorkspace(prob, 16)
+    bad = pages.copy()
+    bad[1] = wl.num_pages
+    with pytest.raises(pkd.PkdError) as e:
+        pws.plan(bad, last)
+    assert e.value.status == -2
+    with pytest.raises(pkd.PkdError) as e:
+        pws.plan(pages, 17)
+    assert e.value.status == -2
+    prob8 = pkd.make_problem(batch=2, num_qo_heads=32, num_kv_heads=8, page_size=8,
+                             dtype="f16", num_pages=100, num_ctas=8)
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.PrefixWorkspace(prob8, 16).plan(np.arange(3, dtype=np.int32), 8)
+    assert e.value.status == -4
+
+
+def test_cascade_shared_prefix_plus_suffix():
+    wl = workloads.cascade()
+    dev = gh.DeviceBatch(wl)
+    prefix = wl.extra_tables["prefix"]
+    pages = prefix.kv_indices[: prefix.kv_indptr[1]]
+    pre_out, pre_lse, plan, st1 = _run_prefix(dev, wl, pages,
+                                              int(prefix.kv_last_page_len[0]))
+    suf_out, suf_lse, _, _, st2 = gh.run_pkd(dev, wl.extra_tables["suffix"])
+    assert st1 == 0 and st2 == 0
+    out, lse = pkd.merge_states(pre_out, pre_lse, suf_out, suf_lse)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(8)
+    total = wl.batch * wl.num_qo_heads
+    rows = np.unique(np.concatenate([rng.choice(total, 300, replace=False),
+                                     [0, total - 1]])).astype(np.int64)
+    ref_out, ref_lse = gh.oracle_ref(wl, rows=rows)
+    print("cascade (shared prefix)", plan.chunks, plan.row_tiles,
+          gh.compare(out, lse, ref_out, ref_lse, wl.dtype, rows=rows))
