@@ -261,6 +261,27 @@ pkd_status pkd_run_static(const pkd_plan_t *plan, const int32_t *host_image,
                           void *out, float *lse, void *stream);
 
 /*
+ * Page append: writes new tokens' key and value rows into the paged cache, the
+ * step before decode ([D] flashinfer.page "Append new K/V tensors to Paged
+ * KV-Cache").  New token i (of num_new) belongs to request
+ * batch_indices_d[i] at position positions_d[i] of that request; the page
+ * table (kv_indptr_d, kv_indices_d, kv_last_page_len_d, for problem->batch
+ * requests) must already cover the requests' new lengths.  k_new / v_new are
+ * [num_new][Hkv][D] of problem->dtype; k_pages / v_pages NHD.  A token outside
+ * its request's length or on a page id outside [0, num_pages) is skipped and
+ * flagged (PKD_DEVICE_BAD_LENGTH / _BAD_PAGE) in *device_status if that
+ * device word is given (may be NULL).  Two new tokens mapping to one slot
+ * race.
+ */
+pkd_status pkd_append_kv(const pkd_problem *problem, const void *k_new,
+                         const void *v_new, const int32_t *batch_indices_d,
+                         const int32_t *positions_d, int64_t num_new, void *k_pages,
+                         void *v_pages, const int32_t *kv_indptr_d,
+                         const int32_t *kv_indices_d,
+                         const int32_t *kv_last_page_len_d, uint32_t *device_status,
+                         void *stream);
+
+/*
  * Shared-prefix (cascade) attention ([W] "Attention states": a shared prefix
  * is evaluated separately from request-specific suffixes and the partial
  * states merged; [D] flashinfer.cascade "Cascade Attention").  The queries of

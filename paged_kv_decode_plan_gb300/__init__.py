@@ -33,7 +33,7 @@ EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
             "pkd_plan_host", "pkd_plan", "pkd_run", "pkd_run_decode",
             "pkd_run_merge", "pkd_merge_states", "pkd_check_status",
             "pkd_run_static", "pkd_prefix_workspace_size", "pkd_plan_shared_prefix",
-            "pkd_run_shared_prefix")
+            "pkd_run_shared_prefix", "pkd_append_kv")
 
 
 class PkdError(RuntimeError):
@@ -103,6 +103,8 @@ def load():
     lib.pkd_check_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.pkd_run_static.argtypes = [ctypes.POINTER(Plan), i32p, vp, vp, vp, vp, vp,
                                    vp, ctypes.c_float, vp, vp, vp]
+    lib.pkd_append_kv.argtypes = [ctypes.POINTER(Problem), vp, vp, vp, vp,
+                                  ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp]
     lib.pkd_prefix_workspace_size.argtypes = [ctypes.POINTER(Problem), ctypes.c_int32,
                                               sz, sz, sz]
     lib.pkd_plan_shared_prefix.argtypes = [ctypes.POINTER(Problem), i32p, ctypes.c_int32,
@@ -113,7 +115,7 @@ def load():
     for name in ("pkd_workspace_size", "pkd_plan_host", "pkd_plan", "pkd_run",
                  "pkd_run_decode", "pkd_run_merge", "pkd_merge_states",
                  "pkd_check_status", "pkd_run_static", "pkd_prefix_workspace_size",
-                 "pkd_plan_shared_prefix", "pkd_run_shared_prefix"):
+                 "pkd_plan_shared_prefix", "pkd_run_shared_prefix", "pkd_append_kv"):
         getattr(lib, name).restype = ctypes.c_int
     if lib.pkd_abi_version() != 2:
         raise RuntimeError("libpkd.so ABI version mismatch")
@@ -303,6 +305,23 @@ def check_status(int_ws, stream=None) -> int:
     if st not in (0, -6):
         _check(st)
     return int(word.value)
+
+
+def append_kv(problem: Problem, k_new, v_new, batch_indices, positions, k_pages,
+              v_pages, kv_indptr, kv_indices, kv_last_page_len, status=None,
+              stream=None):
+    """Writes new tokens' K/V rows ([n, Hkv, D]) into the paged cache."""
+    for t in (k_new, v_new, k_pages, v_pages):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if k_new.dtype != k_pages.dtype or v_new.dtype != v_pages.dtype or \
+            _dtype_code(k_pages.dtype) != problem.dtype:
+        raise ValueError("dtype does not match the problem")
+    _check(load().pkd_append_kv(
+        ctypes.byref(problem), _ptr(k_new), _ptr(v_new), _ptr(batch_indices),
+        _ptr(positions), int(k_new.shape[0]), _ptr(k_pages), _ptr(v_pages),
+        _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(status),
+        _stream_ptr(stream)))
 
 
 def prefix_workspace_size(problem: Problem, max_prefix_pages: int):

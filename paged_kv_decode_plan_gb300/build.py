@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build", platform.machine())
 LIB_PATH = os.path.join(HERE, "libpkd.so")
 
-SOURCES = ["plan.cpp", "api.cu", "decode.cu", "merge.cu", "prefix.cu",
+SOURCES = ["plan.cpp", "api.cu", "decode.cu", "merge.cu", "prefix.cu", "append.cu",
            "static_scratch.cu"]
 HEADERS = ["pkd_internal.h", "ptx.cuh", "kernel_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -250,6 +250,47 @@ pkd_status pkd_merge_states(const void *v_a, const float *s_a, const void *v_b,
   return PKD_OK;
 }
 
+pkd_status pkd_append_kv(const pkd_problem *problem, const void *k_new,
+                         const void *v_new, const int32_t *batch_indices_d,
+                         const int32_t *positions_d, int64_t num_new, void *k_pages,
+                         void *v_pages, const int32_t *kv_indptr_d,
+                         const int32_t *kv_indices_d,
+                         const int32_t *kv_last_page_len_d, uint32_t *device_status,
+                         void *stream) {
+  pkd::clear_error();
+  if (!problem) return fail(PKD_ERR_INVALID_ARG, "null problem");
+  pkd_problem p = *problem;
+  if (p.num_ctas == 0) p.num_ctas = 1;  // not used here
+  pkd_status st = pkd::check_problem(p, false);
+  if (st != PKD_OK) return st;
+  if (num_new < 0) return fail(PKD_ERR_INVALID_ARG, "negative token count");
+  if (num_new == 0) return PKD_OK;
+  if (!k_new || !v_new || !batch_indices_d || !positions_d || !k_pages || !v_pages ||
+      !kv_indptr_d || !kv_indices_d || !kv_last_page_len_d)
+    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+    return fail(PKD_ERR_UNSUPPORTED, "K/V pointers must be 16-byte aligned");
+  pkd::AppendArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.batch_indices = batch_indices_d;
+  a.positions = positions_d;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.kv_indptr = kv_indptr_d;
+  a.kv_indices = kv_indices_d;
+  a.kv_last_page_len = kv_last_page_len_d;
+  a.status = device_status;
+  a.num_new = num_new;
+  a.num_pages = p.num_pages;
+  a.batch = p.batch;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_append(a, stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the append kernel");
+  return PKD_OK;
+}
+
 pkd_status pkd_prefix_workspace_size(const pkd_problem *problem,
                                      int32_t max_prefix_pages, size_t *int_ws_bytes,
                                      size_t *float_ws_bytes, size_t *staging_bytes) {

@@ -108,6 +108,18 @@ struct MergePartialsArgs {
 };
 int launch_merge_partials(const MergePartialsArgs &a, void *stream);
 
+// Page append (append.cu).
+struct AppendArgs {
+  const void *k_new, *v_new;
+  const int32_t *batch_indices, *positions;
+  void *k_pages, *v_pages;
+  const int32_t *kv_indptr, *kv_indices, *kv_last_page_len;
+  uint32_t *status;
+  int64_t num_new, num_pages;
+  int batch, num_kv_heads, page_size;
+};
+int launch_append(const AppendArgs &a, void *stream);
+
 // Shared-prefix attention (prefix.cu) and its chunk merge (merge.cu).
 constexpr int kPrefixMagic = 0x50444B50;  // "PKDP"
 enum PrefixHeaderWord {
