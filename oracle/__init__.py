@@ -92,7 +92,7 @@ class Oracle:
         lib.orc_decode.restype = ctypes.c_int
         lib.orc_decode.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_int, vp, vp, vp, ctypes.c_int64, i32p, i32p, i32p,
+            ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int64, i32p, i32p, i32p,
             ctypes.c_double, i64p, ctypes.c_int64, f64p, f64p]
         lib.orc_merge.restype = ctypes.c_int
         lib.orc_merge.argtypes = [ctypes.c_int64, ctypes.c_int, f64p, f64p,
@@ -106,18 +106,24 @@ class Oracle:
         return int(self.lib.orc_num_threads())
 
     def decode(self, q, k_pages, v_pages, kv_indptr, kv_indices,
-               kv_last_page_len, *, dtype: str, sm_scale: float, rows=None):
+               kv_last_page_len, *, dtype: str, sm_scale: float, rows=None,
+               layout: str = "NHD"):
         """fp64 paged decode attention (page-table walk, two-pass softmax).
 
-        q: [B, Hq, D]; k_pages, v_pages: [num_pages, P, Hkv, D] (NHD).  For
-        f16 / bf16 the arrays hold the 16-bit codes.  ``rows`` optionally
-        lists flattened row ids b * Hq + h.  Returns (out [n, D] float64,
-        lse [n] float64), n = len(rows) or B * Hq.
+        q: [B, Hq, D]; k_pages, v_pages: [num_pages, P, Hkv, D] (NHD) or
+        [num_pages, Hkv, P, D] (HND).  For f16 / bf16 the arrays hold the
+        16-bit codes.  ``rows`` optionally lists flattened row ids b * Hq + h.
+        Returns (out [n, D] float64, lse [n] float64), n = len(rows) or B * Hq.
         """
         if q.ndim != 3 or k_pages.ndim != 4 or v_pages.shape != k_pages.shape:
             raise ValueError("bad tensor ranks / shapes")
         batch, hq, d = q.shape
-        num_pages, page_size, hkv, d2 = k_pages.shape
+        if layout == "HND":
+            num_pages, hkv, page_size, d2 = k_pages.shape
+        elif layout == "NHD":
+            num_pages, page_size, hkv, d2 = k_pages.shape
+        else:
+            raise ValueError("layout must be NHD or HND")
         if d2 != d:
             raise ValueError("head_dim mismatch")
         qr, kr, vr = _raw(q, dtype), _raw(k_pages, dtype), _raw(v_pages, dtype)
@@ -138,7 +144,8 @@ class Oracle:
         if indices.size == 0:
             indices = np.zeros((1,), dtype=np.int32)
         rc = self.lib.orc_decode(
-            batch, hq, hkv, d, page_size, _DTYPE_CODES[dtype], qr.ctypes.data,
+            batch, hq, hkv, d, page_size, _DTYPE_CODES[dtype],
+            1 if layout == "HND" else 0, qr.ctypes.data,
             kr.ctypes.data, vr.ctypes.data, num_pages,
             _ptr(indptr, ctypes.c_int32), _ptr(indices, ctypes.c_int32),
             _ptr(last, ctypes.c_int32), float(sm_scale), rows_p, n,

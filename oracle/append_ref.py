@@ -23,7 +23,7 @@ def request_lengths(kv_indptr, kv_last_page_len, page_size):
 
 
 def append_kv(k_pages, v_pages, k_new, v_new, batch_indices, positions, kv_indptr,
-              kv_indices, kv_last_page_len):
+              kv_indices, kv_last_page_len, layout="NHD"):
     """Writes new rows into copies of the page tensors; returns the copies.
 
     k_pages / v_pages: [num_pages, P, Hkv, D] arrays (any dtype, copied);
@@ -33,7 +33,8 @@ def append_kv(k_pages, v_pages, k_new, v_new, batch_indices, positions, kv_indpt
     """
     k = np.array(k_pages, copy=True)
     v = np.array(v_pages, copy=True)
-    num_pages, page_size = k.shape[0], k.shape[1]
+    num_pages = k.shape[0]
+    page_size = k.shape[2] if layout == "HND" else k.shape[1]
     lengths = request_lengths(kv_indptr, kv_last_page_len, page_size)
     skipped = []
     for i in range(len(batch_indices)):
@@ -46,8 +47,12 @@ def append_kv(k_pages, v_pages, k_new, v_new, batch_indices, positions, kv_indpt
         if page < 0 or page >= num_pages:
             skipped.append(i)
             continue
-        k[page, t % page_size] = k_new[i]
-        v[page, t % page_size] = v_new[i]
+        if layout == "HND":
+            k[page, :, t % page_size] = k_new[i]
+            v[page, :, t % page_size] = v_new[i]
+        else:
+            k[page, t % page_size] = k_new[i]
+            v[page, t % page_size] = v_new[i]
     return k, v, skipped
 
 

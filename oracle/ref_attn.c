@@ -27,8 +27,9 @@
  *    kv_indices[kv_indptr[b] .. kv_indptr[b+1]) in sequence order; every page
  *    is full except the last, which holds kv_last_page_len[b] tokens, 1..P.
  *    A request with no pages has length 0 and its last_page_len is ignored.
- *  - NHD: a page tensor is [num_pages][page_size][num_kv_heads][head_dim],
- *    row-major; K and V are separate tensors of that shape.
+ *  - NHD: a page tensor is [num_pages][page_size][num_kv_heads][head_dim];
+ *    HND: [num_pages][num_kv_heads][page_size][head_dim]; both row-major, K
+ *    and V separate tensors of the same layout.
  *  - Query head h reads key/value head h / g with g = Hq / Hkv.
  *  - Logits include the scale: s_t = sm_scale * <q, k_t>; the log-sum-exp is
  *    the natural logarithm of sum_t exp(s_t).
@@ -46,6 +47,7 @@
 #endif
 
 enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_F64 = 3 };
+enum { ORC_NHD = 0, ORC_HND = 1 };
 
 enum {
   ORC_OK = 0,
@@ -96,6 +98,14 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Element offset of (page, slot, kv head, d = 0) in a page tensor. */
+static int64_t row_base(int layout, int64_t page, int64_t slot, int kvh,
+                        int page_size, int num_kv_heads, int head_dim) {
+  if (layout == ORC_HND)
+    return ((page * num_kv_heads + kvh) * page_size + slot) * head_dim;
+  return ((page * page_size + slot) * num_kv_heads + kvh) * head_dim;
+}
+
 /* Number of tokens of request b under the CSR reading above. */
 static int64_t request_length(const int32_t *kv_indptr,
                               const int32_t *kv_last_page_len, int page_size,
@@ -125,17 +135,17 @@ static int check_table(int batch, int page_size, int64_t num_pages,
 /*
  * Decode attention for the listed rows (row r = b * Hq + h), or for all
  * B * Hq rows when `rows` is NULL.  out is [n_rows][head_dim], lse [n_rows].
- * q is [B][Hq][D]; k_pages and v_pages are NHD page tensors.
+ * q is [B][Hq][D]; k_pages and v_pages are page tensors in `layout`.
  */
 int orc_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
-               int page_size, int dtype, const void *q, const void *k_pages,
+               int page_size, int dtype, int layout, const void *q, const void *k_pages,
                const void *v_pages, int64_t num_pages, const int32_t *kv_indptr,
                const int32_t *kv_indices, const int32_t *kv_last_page_len,
                double sm_scale, const int64_t *rows, int64_t n_rows,
                double *out, double *lse) {
   if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       page_size <= 0 || num_qo_heads % num_kv_heads != 0 || dtype < ORC_F16 ||
-      dtype > ORC_F64)
+      dtype > ORC_F64 || (layout != ORC_NHD && layout != ORC_HND))
     return ORC_ERR_ARG;
   int rc = check_table(batch, page_size, num_pages, kv_indptr, kv_indices,
                        kv_last_page_len);
@@ -174,7 +184,7 @@ int orc_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
       int64_t page = kv_indices[kv_indptr[b] + t / page_size];
       int64_t slot = t % page_size;
       int64_t k_base =
-          ((page * page_size + slot) * num_kv_heads + kvh) * head_dim;
+          row_base(layout, page, slot, kvh, page_size, num_kv_heads, head_dim);
       double dot = 0.0;
       for (int d = 0; d < head_dim; ++d)
         dot += element(q, dtype, q_base + d) * element(k_pages, dtype, k_base + d);
@@ -190,7 +200,7 @@ int orc_decode(int batch, int num_qo_heads, int num_kv_heads, int head_dim,
       int64_t page = kv_indices[kv_indptr[b] + t / page_size];
       int64_t slot = t % page_size;
       int64_t v_base =
-          ((page * page_size + slot) * num_kv_heads + kvh) * head_dim;
+          row_base(layout, page, slot, kvh, page_size, num_kv_heads, head_dim);
       for (int d = 0; d < head_dim; ++d)
         o[d] += w * element(v_pages, dtype, v_base + d);
     }

@@ -287,7 +287,28 @@ def check_wide_spread(orc):
             <= 1e-9, "wide spread lse"
 
 
-ALL_CHECKS = [check_bruteforce, check_wide_spread, check_single_key, check_identical_keys,
+def check_hnd_layout(orc):
+    """HND copies of NHD pools (per page: heads before slots) give the same
+    states, bit for bit; an NHD pool read as HND does not."""
+    rng = np.random.default_rng(19)
+    for p in (1, 3, 8):
+        case = paged_case(rng, [2 * p + 1, 5 * p, 1], 8, 4, 16, p, "bf16")
+        out, lse = run_case(orc, case)
+        k_hnd = np.ascontiguousarray(case["k"].transpose(0, 2, 1, 3))
+        v_hnd = np.ascontiguousarray(case["v"].transpose(0, 2, 1, 3))
+        out2, lse2 = orc.decode(case["q"], k_hnd, v_hnd, case["indptr"],
+                                case["indices"], case["last"], dtype="bf16",
+                                sm_scale=case["sm_scale"], layout="HND")
+        assert np.array_equal(out, out2) and np.array_equal(lse, lse2), "HND copy"
+        if p > 1:
+            out3, _ = orc.decode(case["q"], case["k"].reshape(k_hnd.shape),
+                                 case["v"].reshape(v_hnd.shape), case["indptr"],
+                                 case["indices"], case["last"], dtype="bf16",
+                                 sm_scale=case["sm_scale"], layout="HND")
+            assert not np.allclose(out, out3), "layout flag ignored"
+
+
+ALL_CHECKS = [check_bruteforce, check_wide_spread, check_hnd_layout, check_single_key, check_identical_keys,
               check_gqa_mapping, check_union, check_empty, check_permutation,
               check_extreme_shift]
 

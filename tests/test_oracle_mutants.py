@@ -17,8 +17,11 @@ MUTANTS = {
     "slot_off_by_one": ("int64_t slot = t % page_size;\n      int64_t k_base",
                         "int64_t slot = (t + 1) % page_size;\n      int64_t k_base"),
     "hnd_instead_of_nhd": (
-        "((page * page_size + slot) * num_kv_heads + kvh) * head_dim;\n      double dot",
-        "((page * num_kv_heads + kvh) * page_size + slot) * head_dim;\n      double dot"),
+        "  return ((page * page_size + slot) * num_kv_heads + kvh) * head_dim;",
+        "  return ((page * num_kv_heads + kvh) * page_size + slot) * head_dim;"),
+    "hnd_head_and_slot_swapped": (
+        "    return ((page * num_kv_heads + kvh) * page_size + slot) * head_dim;",
+        "    return ((page * page_size + slot) * num_kv_heads + kvh) * head_dim;"),
     "scale_dropped": ("s[t] = sm_scale * dot;", "s[t] = dot;"),
     "lse_without_max": ("lse[i] = m + log(z);", "lse[i] = log(z);"),
     "finite_sentinel": ("double m = -INFINITY;\n    for (int64_t t",
