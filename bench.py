@@ -216,7 +216,7 @@ class Runner:
     previous step still runs; the decode launch waits only for its own copy.
     """
 
-    def __init__(self, wl, device, kv_loader=0, cascade="shared"):
+    def __init__(self, wl, device, kv_loader=0, cascade="shared", layout="nhd"):
         import torch
         import paged_kv_decode_plan_gb300 as pkd
         self.torch = torch
@@ -226,6 +226,10 @@ class Runner:
         self.q = wl.q.to(device)
         self.k = wl.k_pages.to(device)
         self.v = wl.v_pages.to(device)
+        self.layout = pkd.LAYOUT_HND if layout == "hnd" else pkd.LAYOUT_NHD
+        if layout == "hnd":  # same values, [pages][Hkv][P][D]
+            self.k = self.k.transpose(1, 2).contiguous()
+            self.v = self.v.transpose(1, 2).contiguous()
         # cascade: the shared prefix once through the shared-prefix kernel
         # ("shared"), or listed in every request's table ("per-request")
         self.shared = wl.name == "cascade" and cascade == "shared"
@@ -241,7 +245,8 @@ class Runner:
             pages = pt.kv_indices[: pt.kv_indptr[1]].copy()
             prob = pkd.make_problem(batch=pt.batch, num_qo_heads=wl.num_qo_heads,
                                     num_kv_heads=wl.num_kv_heads, page_size=pt.page_size,
-                                    dtype=wl.dtype, num_pages=wl.num_pages)
+                                    dtype=wl.dtype, num_pages=wl.num_pages,
+                                    kv_layout=self.layout)
             self.prefix = dict(
                 pages=pages, last=int(pt.kv_last_page_len[0]),
                 ws=[pkd.PrefixWorkspace(prob, pages.size, device=device) for _ in range(2)],
@@ -253,7 +258,7 @@ class Runner:
                                     num_kv_heads=wl.num_kv_heads, page_size=t.page_size,
                                     dtype=wl.dtype, num_pages=wl.num_pages,
                                     min_chunks_per_request=wl.min_chunks_per_request,
-                                    kv_loader=kv_loader)
+                                    kv_loader=kv_loader, kv_layout=self.layout)
             ws = [pkd.Workspace(prob, device=device) for _ in range(2)]
             dev = tuple(torch.from_numpy(a).to(device) for a in
                         (t.kv_indptr, t.kv_indices, t.kv_last_page_len))
@@ -361,7 +366,7 @@ def run_ours(args, ranks):
     device = torch.device("cuda", ranks.local)
     wl = make_workload(args)
     runner = Runner(wl, device, kv_loader={"auto": 0, "tma": 1, "bulk": 2}[args.loader],
-                    cascade=args.cascade)
+                    cascade=args.cascade, layout=args.layout)
     stream = torch.cuda.current_stream()
 
     # host plan time (median of 20)
@@ -441,6 +446,7 @@ def run_ours(args, ranks):
         "num_units": runner.parts[0]["plan"].num_units,
         "num_split_requests": runner.parts[0]["plan"].num_split_requests,
         "kv_loader": args.loader,
+        "kv_layout": args.layout,
         "cascade": (args.cascade if wl.name == "cascade" else None),
         "prefix_us": (round(statistics.fmean(prefix_ms) * 1e3, 2)
                       if prefix_ms else None),
@@ -617,6 +623,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(DESCRIPTIONS), default="batch64")
     ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--layout", choices=["nhd", "hnd"], default="nhd",
+                    help="page tensor layout (the same values either way)")
     ap.add_argument("--cascade", choices=["shared", "per-request"], default="shared",
                     help="cascade workload: shared-prefix kernel, or the prefix "
                          "pages listed in every request's table")

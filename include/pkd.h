@@ -16,7 +16,8 @@
  * g = Hq / Hkv, D = head_dim, P = page_size):
  *  q          [B][Hq][D]                      dtype
  *  k_pages    [num_pages][P][Hkv][D]          dtype  (NHD, [D] tutorial
- *  v_pages    [num_pages][P][Hkv][D]          dtype   "KV-Cache Layout")
+ *  v_pages    [num_pages][P][Hkv][D]          dtype   "KV-Cache Layout"), or
+ *             [num_pages][Hkv][P][D] with problem.kv_layout = PKD_LAYOUT_HND
  *  kv_indptr  [B + 1] int32, kv_indices [kv_indptr[B]] int32,
  *  kv_last_page_len [B] int32: CSR page table ([D] "Page Table Layout";
  *    [W] "Block-sparse cache representation").  Request b owns pages
@@ -61,11 +62,19 @@ typedef enum {
 
 typedef enum { PKD_F16 = 0, PKD_BF16 = 1, PKD_F32 = 2 } pkd_dtype;
 
+/* Page tensor layouts ([D] "KV-Cache Layout in FlashInfer", "Layout: NHD/HND"). */
+typedef enum {
+  PKD_LAYOUT_NHD = 0,  /* [num_pages][page_size][num_kv_heads][head_dim] */
+  PKD_LAYOUT_HND = 1   /* [num_pages][num_kv_heads][page_size][head_dim] */
+} pkd_layout;
+
 /* How the decode kernel moves K/V pages into shared memory. */
 typedef enum {
-  PKD_LOADER_AUTO = 0,       /* the library's choice: bulk rows */
+  PKD_LOADER_AUTO = 0,       /* the library's choice: bulk rows for NHD; for HND,
+                                TMA tiles when page_size % 16 == 0, else bulk rows */
   PKD_LOADER_TMA_TILES = 1,  /* TMA tiled loads of 16-token boxes (page_size % 16 == 0) */
-  PKD_LOADER_BULK_ROWS = 2   /* one bulk copy per token row of all heads (any page_size) */
+  PKD_LOADER_BULK_ROWS = 2   /* one bulk copy per token row of all heads (NHD) or per
+                                (token, head) row (HND); any page_size */
 } pkd_loader;
 
 /* Bits of the device status word (see pkd_check_status). */
@@ -92,7 +101,7 @@ typedef struct {
                             kernel's tile); other values are unsupported */
   int32_t max_batch;     /* capacity used to size workspaces; 0 = batch */
   int32_t kv_loader;     /* pkd_loader */
-  int32_t reserved;      /* 0 */
+  int32_t kv_layout;     /* pkd_layout of k_pages and v_pages */
 } pkd_problem;
 
 /* Result of planning: plain data, owned and stored by the caller. */

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libpkd.so")
 
 PKD_F16, PKD_BF16, PKD_F32 = 0, 1, 2
 LOADER_AUTO, LOADER_TMA_TILES, LOADER_BULK_ROWS = 0, 1, 2
+LAYOUT_NHD, LAYOUT_HND = 0, 1
 DEVICE_BAD_PAGE, DEVICE_BAD_LENGTH, DEVICE_BAD_PLAN, DEVICE_TIMEOUT = 1, 2, 4, 8
 STATUS_NAMES = {0: "PKD_OK", -1: "PKD_ERR_INVALID_ARG", -2: "PKD_ERR_PAGE_TABLE",
                 -3: "PKD_ERR_WORKSPACE", -4: "PKD_ERR_UNSUPPORTED",
@@ -49,7 +50,7 @@ class Problem(ctypes.Structure):
                 ("num_pages", ctypes.c_int64), ("num_ctas", ctypes.c_int32),
                 ("min_chunks_per_request", ctypes.c_int32),
                 ("tile_tokens", ctypes.c_int32), ("max_batch", ctypes.c_int32),
-                ("kv_loader", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("kv_loader", ctypes.c_int32), ("kv_layout", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -143,10 +144,12 @@ def _dtype_code(dtype) -> int:
 
 def make_problem(*, batch, num_qo_heads, num_kv_heads, page_size, dtype,
                  num_pages, head_dim=128, num_ctas=0, min_chunks_per_request=1,
-                 tile_tokens=0, max_batch=0, kv_loader=LOADER_AUTO) -> Problem:
+                 tile_tokens=0, max_batch=0, kv_loader=LOADER_AUTO,
+                 kv_layout=LAYOUT_NHD) -> Problem:
     return Problem(batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                    _dtype_code(dtype), num_pages, num_ctas,
-                   min_chunks_per_request, tile_tokens, max_batch, kv_loader, 0)
+                   min_chunks_per_request, tile_tokens, max_batch, kv_loader,
+                   {"NHD": LAYOUT_NHD, "HND": LAYOUT_HND}.get(kv_layout, kv_layout))
 
 
 def workspace_size(problem: Problem):

@@ -168,6 +168,7 @@ pkd_status pkd_run_decode(const pkd_plan_t *plan, const void *q,
   a.max_partials = bounds.max_partials;
   a.image_words = bounds.image_words;
   a.loader = p.kv_loader;
+  a.layout = p.kv_layout;
   cudaError_t e = static_cast<cudaError_t>(pkd::launch_decode(a, stream));
   if (e == cudaErrorNotSupported)
     return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");
@@ -286,6 +287,7 @@ pkd_status pkd_append_kv(const pkd_problem *problem, const void *k_new,
   a.batch = p.batch;
   a.num_kv_heads = p.num_kv_heads;
   a.page_size = p.page_size;
+  a.layout = p.kv_layout;
   cudaError_t e = static_cast<cudaError_t>(pkd::launch_append(a, stream));
   if (e != cudaSuccess) return cuda_fail(e, "launching the append kernel");
   return PKD_OK;
@@ -374,6 +376,7 @@ pkd_status pkd_run_shared_prefix(const pkd_prefix_plan_t *plan, const void *q,
   a.chunks = plan->chunks;
   a.chunk_tiles = plan->chunk_tiles;
   a.row_tiles = plan->row_tiles;
+  a.layout = p.kv_layout;
   cudaError_t e = static_cast<cudaError_t>(pkd::launch_shared_prefix(a, stream));
   if (e == cudaErrorNotSupported)
     return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");

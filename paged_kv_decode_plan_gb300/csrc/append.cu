@@ -23,7 +23,7 @@ struct AppendParams {
   const int32_t *indptr, *indices, *last;
   uint32_t *status;
   long long num_new, num_pages;
-  int batch, hkv, page_size;
+  int batch, hkv, page_size, hnd;
 };
 
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
@@ -62,9 +62,20 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(
         (tensor ? p.v_new : p.k_new) + i * p.hkv * kHeadDim);
-    uint4 *dst = reinterpret_cast<uint4 *>((tensor ? p.v_pages : p.k_pages) +
-                                           row * p.hkv * kHeadDim);
-    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+    uint16_t *pages = tensor ? p.v_pages : p.k_pages;
+    if (p.hnd) {
+      // HND: head h's row of this token is at ((page * Hkv + h) * P + slot)
+      const long long page = row / p.page_size, slot = row - page * p.page_size;
+      for (int c = lane; c < chunks; c += 32) {
+        const int h = c >> 4, w = c & 15;
+        reinterpret_cast<uint4 *>(
+            pages + ((page * p.hkv + h) * p.page_size + slot) * kHeadDim)[w] =
+            __ldg(src + c);
+      }
+    } else {
+      uint4 *dst = reinterpret_cast<uint4 *>(pages + row * p.hkv * kHeadDim);
+      for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+    }
   }
 }
 
@@ -88,6 +99,7 @@ int launch_append(const AppendArgs &a, void *stream) {
   p.batch = a.batch;
   p.hkv = a.num_kv_heads;
   p.page_size = a.page_size;
+  p.hnd = a.layout == PKD_LAYOUT_HND;
   const long long warps = 2 * a.num_new;
   const long long want = (warps + 7) / 8;
   const int grid = static_cast<int>(want < 65535LL * 8 ? want : 65535LL * 8);

@@ -92,6 +92,7 @@ struct Params {
   int max_partials;   // partial slots the float workspace holds
   int image_words;    // int32 words the image may span
   int grid;           // CTAs launched
+  int hnd;            // page tensors are HND
   // batch: requests the q / out / lse / page-table buffers hold; a plan may
   // cover fewer (a captured launch replayed with a later, smaller plan)
 };
@@ -192,8 +193,12 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
         const int half = lane & 1;
         const uint32_t dst = stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
                              head * G::kHeadBytes + half * kHalfBytes;
-        ptx::tma_load_3d(dst, tensor ? map_v : map_k, half * 64, head,
-                         page * p.page_size + slot0, full0 + 8 * s);
+        if (p.hnd)
+          ptx::tma_load_4d(dst, tensor ? map_v : map_k, half * 64, slot0, head, page,
+                           full0 + 8 * s);
+        else
+          ptx::tma_load_3d(dst, tensor ? map_v : map_k, half * 64, head,
+                           page * p.page_size + slot0, full0 + 8 * s);
       }
       ++it;
     }
@@ -204,7 +209,8 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
 }
 
 // One 1-D bulk copy per (tensor, token) row: lane l moves row l & 15 of K
-// (l < 16) or V (l >= 16); page ids are loaded one tile ahead.
+// (l < 16) or V (l >= 16); for HND pages one copy per (tensor, token, head).
+// Page ids are loaded one tile ahead.
 template <int HKV>
 __device__ void load_bulk(const Params &p, const int32_t *units, int num_partials,
                           int u_begin, int u_end, uint8_t *stages, uint32_t full0,
@@ -262,11 +268,22 @@ __device__ void load_bulk(const Params &p, const int32_t *units, int num_partial
         flag(p.image, PKD_DEVICE_BAD_PAGE);
         pg = 0;
       }
-      const uint16_t *src =
-          base + (static_cast<long long>(pg) * p.page_size + slot) * HKV * kHeadDim;
-      ptx::bulk_load(stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
-                         r * G::kRowStride,
-                     src, kRow, full0 + 8 * s);
+      const uint32_t dst =
+          stage0 + s * G::kStageBytes + tensor * G::kTensorBytes + r * G::kRowStride;
+      if (p.hnd) {
+        // HND: the token's head rows are P * 256 bytes apart
+#pragma unroll
+        for (int h = 0; h < HKV; ++h)
+          ptx::bulk_load(dst + h * kRowBytes,
+                         base + ((static_cast<long long>(pg) * HKV + h) * p.page_size +
+                                 slot) * kHeadDim,
+                         kRowBytes, full0 + 8 * s);
+      } else {
+        ptx::bulk_load(dst,
+                       base + (static_cast<long long>(pg) * p.page_size + slot) * HKV *
+                                  kHeadDim,
+                       kRow, full0 + 8 * s);
+      }
     }
     describe();
     ++it;
@@ -631,16 +648,29 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// K or V pages viewed as [token row][head][d] with d innermost; boxes of 16
-// token rows x 1 head x 64 elements, 128-byte swizzle.
+// K or V pages with d innermost: NHD as [token row][head][d] (3-D), HND as
+// [page][head][slot][d] (4-D); boxes of 16 token rows x 1 head x 64
+// elements, 128-byte swizzle.
 bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
-                  int page_size, int hkv) {
+                  int page_size, int hkv, int layout) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return false;
+  const cuuint64_t row = kRowBytes;
+  if (layout == PKD_LAYOUT_HND) {
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim),
+                          static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(hkv),
+                          static_cast<cuuint64_t>(num_pages)};
+    cuuint64_t strides[3] = {row, row * page_size, row * page_size * hkv};
+    cuuint32_t box[4] = {64, kTile, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(hkv),
                         static_cast<cuuint64_t>(num_pages) * page_size};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBytes),
-                           static_cast<cuuint64_t>(kRowBytes) * hkv};
+  cuuint64_t strides[2] = {row, row * hkv};
   cuuint32_t box[3] = {64, 1, kTile};
   cuuint32_t estr[3] = {1, 1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(base), dims,
@@ -652,11 +682,11 @@ bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
 // Tensor maps of the last page pools seen (encoding is pure host work, but a
 // serving loop passes the same pools on every step).
 bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
-                 long long num_pages, int page_size, int hkv) {
+                 long long num_pages, int page_size, int hkv, int layout) {
   struct Entry {
     const void *k, *v;
     long long num_pages;
-    int page_size, hkv;
+    int page_size, hkv, layout;
     alignas(64) CUtensorMap mk;
     alignas(64) CUtensorMap mv;
   };
@@ -666,14 +696,14 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
   std::lock_guard<std::mutex> lock(mutex);
   for (const Entry &e : cache)
     if (e.k == k && e.v == v && e.num_pages == num_pages && e.page_size == page_size &&
-        e.hkv == hkv && e.k) {
+        e.hkv == hkv && e.layout == layout && e.k) {
       *mk = e.mk;
       *mv = e.mv;
       return true;
     }
   Entry &e = cache[next];
-  if (!encode_pages(&e.mk, k, num_pages, page_size, hkv) ||
-      !encode_pages(&e.mv, v, num_pages, page_size, hkv)) {
+  if (!encode_pages(&e.mk, k, num_pages, page_size, hkv, layout) ||
+      !encode_pages(&e.mv, v, num_pages, page_size, hkv, layout)) {
     e.k = nullptr;
     return false;
   }
@@ -682,6 +712,7 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
   e.num_pages = num_pages;
   e.page_size = page_size;
   e.hkv = hkv;
+  e.layout = layout;
   next = (next + 1) % 8;
   *mk = e.mk;
   *mv = e.mv;
@@ -691,8 +722,8 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
 }  // namespace
 
 bool page_tensor_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
-                      long long num_pages, int page_size, int hkv) {
-  return cached_maps(mk, mv, k, v, num_pages, page_size, hkv);
+                      long long num_pages, int page_size, int hkv, int layout) {
+  return cached_maps(mk, mv, k, v, num_pages, page_size, hkv, layout);
 }
 
 int launch_decode(const DecodeArgs &a, void *stream) {
@@ -716,19 +747,25 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   prm.max_partials = a.max_partials;
   prm.image_words = a.image_words;
   prm.grid = a.num_ctas;
+  prm.hnd = a.layout == PKD_LAYOUT_HND;
 
   alignas(64) CUtensorMap mk;
   alignas(64) CUtensorMap mv;
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
-  // bulk rows unless TMA tiles were asked for; TMA tiles need every tile
-  // inside one page and token rows that fit in int32
+  // NHD: bulk rows unless TMA tiles were asked for.  HND: TMA tiles when
+  // pages hold whole 16-token tiles (a token's head rows are P * 256 bytes
+  // apart there, so a bulk row is one head).  TMA tiles need every tile
+  // inside one page and token rows that fit in int32.
+  const bool tiles_fit = a.page_size % kTile == 0 && a.num_pages > 0 &&
+                         a.num_pages * static_cast<long long>(a.page_size) < (1ll << 31);
+  const bool want_tma =
+      a.loader == PKD_LOADER_TMA_TILES ||
+      (a.loader == PKD_LOADER_AUTO && a.layout == PKD_LAYOUT_HND && tiles_fit);
   int loader = kLoaderBulk;
-  if (a.loader == PKD_LOADER_TMA_TILES) {
-    if (a.page_size % kTile != 0 || a.num_pages <= 0 ||
-        a.num_pages * static_cast<long long>(a.page_size) >= (1ll << 31) ||
-        !cached_maps(&mk, &mv, a.k_pages, a.v_pages, a.num_pages, a.page_size,
-                     a.num_kv_heads))
+  if (want_tma) {
+    if (!tiles_fit || !cached_maps(&mk, &mv, a.k_pages, a.v_pages, a.num_pages,
+                                   a.page_size, a.num_kv_heads, a.layout))
       return cudaErrorNotSupported;
     loader = kLoaderTma;
   }

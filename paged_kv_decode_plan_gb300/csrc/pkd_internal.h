@@ -94,6 +94,7 @@ struct DecodeArgs {
   int batch, num_qo_heads, num_kv_heads, page_size, num_ctas, dtype;
   int max_partials, image_words;
   int loader;  // pkd_loader of the problem
+  int layout;  // pkd_layout of the page tensors
 };
 int launch_decode(const DecodeArgs &a, void *stream);
 
@@ -116,7 +117,7 @@ struct AppendArgs {
   const int32_t *kv_indptr, *kv_indices, *kv_last_page_len;
   uint32_t *status;
   int64_t num_new, num_pages;
-  int batch, num_kv_heads, page_size;
+  int batch, num_kv_heads, page_size, layout;
 };
 int launch_append(const AppendArgs &a, void *stream);
 
@@ -134,6 +135,7 @@ struct PrefixArgs {
   int64_t num_pages;
   int batch, num_qo_heads, num_kv_heads, page_size, dtype;
   int length, chunks, chunk_tiles, row_tiles;
+  int layout;
 };
 int launch_shared_prefix(const PrefixArgs &a, void *stream);
 int prefix_tile_tokens();
@@ -146,12 +148,13 @@ pkd_status plan_prefix_impl(const pkd_problem &in, const int32_t *pages,
 void prefix_workspace_bytes(const pkd_problem &p, int32_t max_prefix_pages,
                             size_t *int_ws, size_t *float_ws, size_t *staging);
 
-// Tensor maps for K and V page pools viewed as [token row][head][d]: boxes of
-// 16 token rows x 1 head x 64 elements, 128-byte swizzle; cached per pool.
-// (CUtensorMap comes from <cuda.h>; callers include it first.)
+// Tensor maps for K and V page pools: NHD viewed as [token row][head][d]
+// (3-D), HND as [page][head][slot][d] (4-D); boxes of 16 token rows x 1 head x
+// 64 elements, 128-byte swizzle; cached per pool.  (CUtensorMap comes from
+// <cuda.h>; callers include it first.)
 #ifdef CUDA_VERSION
 bool page_tensor_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
-                      long long num_pages, int page_size, int hkv);
+                      long long num_pages, int page_size, int hkv, int layout);
 #endif
 
 int launch_merge_states(const void *v_a, const float *s_a, const void *v_b,

@@ -61,6 +61,8 @@ pkd_status check_problem(const pkd_problem &p, bool need_ctas) {
     return fail(PKD_ERR_UNSUPPORTED, "query group larger than 16");
   if (p.tile_tokens != 0 && p.tile_tokens != kTileTokens)
     return fail(PKD_ERR_UNSUPPORTED, "tile_tokens must be 0 or 16");
+  if (p.kv_layout != PKD_LAYOUT_NHD && p.kv_layout != PKD_LAYOUT_HND)
+    return fail(PKD_ERR_INVALID_ARG, "kv_layout must be a pkd_layout value");
   if (p.kv_loader < PKD_LOADER_AUTO || p.kv_loader > PKD_LOADER_BULK_ROWS)
     return fail(PKD_ERR_INVALID_ARG, "kv_loader must be a pkd_loader value");
   if (p.kv_loader == PKD_LOADER_TMA_TILES && p.page_size % kTileTokens != 0)

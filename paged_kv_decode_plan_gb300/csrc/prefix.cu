@@ -52,6 +52,7 @@ struct PrefixParams {
   long long num_pages;
   int batch, hq, hkv, group, page_size;
   int length, chunks, chunk_tiles, row_tiles;
+  int hnd;                // page tensors are HND
 };
 
 __device__ __forceinline__ void give_up(const PrefixParams &p, volatile int *abort) {
@@ -89,8 +90,13 @@ __device__ void load_prefix(const PrefixParams &p, const CUtensorMap *map_k,
       }
       const uint32_t dst = stage0 + s * kPStageBytes + tensor * kPTensorBytes +
                            sub * 2 * kHalfBytes + half * kHalfBytes;
-      ptx::tma_load_3d(dst, tensor ? map_v : map_k, half * 64, h,
-                       page * p.page_size + (tok - pi * p.page_size), full0 + 8 * s);
+      const int slot = tok - pi * p.page_size;
+      if (p.hnd)
+        ptx::tma_load_4d(dst, tensor ? map_v : map_k, half * 64, slot, h, page,
+                         full0 + 8 * s);
+      else
+        ptx::tma_load_3d(dst, tensor ? map_v : map_k, half * 64, h,
+                         page * p.page_size + slot, full0 + 8 * s);
     }
   }
   for (int j = max(0, it - kPStages); j < it; ++j)
@@ -349,7 +355,7 @@ int launch_shared_prefix(const PrefixArgs &a, void *stream) {
   alignas(64) CUtensorMap mk;
   alignas(64) CUtensorMap mv;
   if (!page_tensor_maps(&mk, &mv, a.k_pages, a.v_pages, a.num_pages, a.page_size,
-                        a.num_kv_heads))
+                        a.num_kv_heads, a.layout))
     return cudaErrorNotSupported;
   PrefixParams p;
   p.q = static_cast<const uint16_t *>(a.q);
@@ -367,6 +373,7 @@ int launch_shared_prefix(const PrefixArgs &a, void *stream) {
   p.chunks = a.chunks;
   p.chunk_tiles = a.chunk_tiles;
   p.row_tiles = a.row_tiles;
+  p.hnd = a.layout == PKD_LAYOUT_HND;
   const int grid = a.num_kv_heads * a.row_tiles * a.chunks;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;

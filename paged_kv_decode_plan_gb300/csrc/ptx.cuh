@@ -141,6 +141,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tensor_map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tensor_map,
+                                            int c0, int c1, int c2, int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(bar)
+      : "memory");
+}
+
 // ---- TMA: 1-D bulk copy global -> shared, completion on an mbarrier ------
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
