@@ -311,7 +311,7 @@ typedef struct {
   int32_t prefix_num_pages;
   int32_t chunks;               /* KV chunks of the prefix (partial states per row) */
   int32_t chunk_tiles;          /* 64-token tiles per chunk */
-  int32_t row_tiles;            /* 128-row tiles per key/value head */
+  int32_t row_tiles;            /* 256-row tiles per key/value head */
   int32_t num_blocks;           /* CTAs of the prefix kernel */
   int64_t int_ws_bytes_used;    /* bytes of the prefix plan image */
   int64_t float_ws_bytes_needed;/* bytes of fp32 partial states */

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(HERE, "libpkd.so")
 
 SOURCES = ["plan.cpp", "api.cu", "decode.cu", "merge.cu", "prefix.cu", "append.cu",
            "static_scratch.cu"]
-HEADERS = ["pkd_internal.h", "ptx.cuh", "kernel_common.cuh"]
+HEADERS = ["pkd_internal.h", "ptx.cuh", "kernel_common.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
           "-I" + INCLUDE, "-I" + CSRC]

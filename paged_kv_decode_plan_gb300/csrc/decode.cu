@@ -726,6 +726,20 @@ bool page_tensor_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const voi
   return cached_maps(mk, mv, k, v, num_pages, page_size, hkv, layout);
 }
 
+bool query_tensor_map(CUtensorMap *map, const void *q, int batch, int hq, int group) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode || group < 1 || 128 % group != 0 || batch < 1) return false;
+  const cuuint64_t row = kRowBytes;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(hq),
+                        static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[2] = {row, row * hq};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(128 / group)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(q), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int launch_decode(const DecodeArgs &a, void *stream) {
   Params prm;
   prm.q = static_cast<const uint16_t *>(a.q);

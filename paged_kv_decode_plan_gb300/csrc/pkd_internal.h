@@ -138,8 +138,6 @@ struct PrefixArgs {
   int layout;
 };
 int launch_shared_prefix(const PrefixArgs &a, void *stream);
-int prefix_tile_tokens();
-int prefix_tile_rows();
 int launch_merge_uniform(const float *partials, void *out, float *lse, int batch, int hq,
                          int chunks, int dtype, int grid, void *stream);
 pkd_status plan_prefix_impl(const pkd_problem &in, const int32_t *pages,
@@ -155,6 +153,10 @@ void prefix_workspace_bytes(const pkd_problem &p, int32_t max_prefix_pages,
 #ifdef CUDA_VERSION
 bool page_tensor_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
                       long long num_pages, int page_size, int hkv, int layout);
+// Queries [batch][hq][d] as a 3-D map with boxes of 64 elements x `group`
+// heads x 128 / group requests (128 query rows of one key/value head, in
+// request-major order), 128-byte swizzle.  False when 128 % group != 0.
+bool query_tensor_map(CUtensorMap *map, const void *q, int batch, int hq, int group);
 #endif
 
 int launch_merge_states(const void *v_a, const float *s_a, const void *v_b,

@@ -107,3 +107,31 @@ def test_cascade_shared_prefix_plus_suffix():
     ref_out, ref_lse = gh.oracle_ref(wl, rows=rows)
     print("cascade (shared prefix)", plan.chunks, plan.row_tiles,
           gh.compare(out, lse, ref_out, ref_lse, wl.dtype, rows=rows))
+
+
+@pytest.mark.parametrize("dtype,length,ctas", [("f16", 3000, 8), ("bf16", 1500, 4),
+                                               ("f16", 700, 152)])
+def test_shared_prefix_growing_scores(dtype, length, ctas):
+    # keys grow along the prefix, so the running maximum keeps rising and the
+    # reference moves (rescaling the accumulated output) after the first tile
+    batch = 6
+    wl, pages, last, table = _prefix_case(batch, 32, 8, 16, length, dtype, seed=length)
+    k = wl.k_pages.float()
+    for t in range(length):
+        k[pages[t // 16], t % 16] *= 1.0 + 7.0 * t / length
+    wl.k_pages = k.to(wl.k_pages.dtype)
+    dev = gh.DeviceBatch(wl)
+    out, lse, plan, status = _run_prefix(dev, wl, pages, last, ctas)
+    assert status == 0
+    ref_out, ref_lse = gh.oracle_ref(wl, table=table)
+    gh.compare(out, lse, ref_out, ref_lse, dtype)
+    # the last tokens dominate: the growth really moved the maximum
+    assert float(ref_lse.max()) > 8.0
+
+
+def test_shared_prefix_empty():
+    wl, _, _, _ = _prefix_case(3, 32, 8, 16, 16, "f16", seed=5)
+    dev = gh.DeviceBatch(wl)
+    out, lse, plan, status = _run_prefix(dev, wl, np.zeros(0, np.int32), 0)
+    assert status == 0 and plan.prefix_len == 0
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
