@@ -135,3 +135,28 @@ def test_shared_prefix_empty():
     out, lse, plan, status = _run_prefix(dev, wl, np.zeros(0, np.int32), 0)
     assert status == 0 and plan.prefix_len == 0
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_shared_prefix_single_dominant_token(dtype):
+    # one prefix key points along query row (request 0, head 0): that row's
+    # weights collapse onto a single token, so its output is one value row and
+    # any mismatch between the normaliser and the rounded weights shows
+    batch, length = 4, 700
+    wl, pages, last, table = _prefix_case(batch, 32, 8, 16, length, dtype, seed=41)
+    q0 = wl.q[0, 0].float()
+    k = wl.k_pages.float()
+    v = wl.v_pages.float()
+    t_star = 333
+    k[pages[t_star // 16], t_star % 16, 0] = q0 * (4.0 / q0.norm()) * (128 ** 0.5)
+    v[pages[t_star // 16], t_star % 16, 0] = torch.linspace(-4.5, 4.5, 128)
+    wl.k_pages = k.to(wl.k_pages.dtype)
+    wl.v_pages = v.to(wl.v_pages.dtype)
+    dev = gh.DeviceBatch(wl)
+    out, lse, plan, status = _run_prefix(dev, wl, pages, last, 8)
+    assert status == 0
+    ref_out, ref_lse = gh.oracle_ref(wl, table=table)
+    gh.compare(out, lse, ref_out, ref_lse, dtype)
+    # the row really is dominated by that token
+    v_star = wl.v_pages[pages[t_star // 16], t_star % 16, 0].float().numpy()
+    assert np.abs(ref_out[0] - v_star).max() < 1e-3
