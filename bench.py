@@ -3,7 +3,8 @@
 
 One step = one pass of the whole hot path over one synthetic batch: plan on
 the host (lengths -> split-KV work list -> H2D copy of the plan image), the
-decode kernel, and the split-KV merge kernel.  The default workload is the
+decode kernel, and the split-KV merge kernel (by default replayed as one CUDA
+graph per workspace; ``--graph off`` launches them one by one).  The default workload is the
 64-request batch (lengths uniform on [128, 4096], Hq 32 / Hkv 8, head_dim 128,
 page_size 16, fp16); ``--workload`` selects another of
 paged_kv_decode_plan_gb300.workloads.
@@ -214,9 +215,13 @@ class Runner:
     Serving-loop pipelining: two workspaces per table alternate between
     steps, and each step's plan image is copied on a side stream while the
     previous step still runs; the decode launch waits only for its own copy.
+    With ``graph``, the kernel launches of a step are one CUDA graph per
+    workspace (captured after the eager warm-up, valid for every later plan of
+    the same capacity); planning and the plan copies stay on the host per step.
     """
 
-    def __init__(self, wl, device, kv_loader=0, cascade="shared", layout="nhd"):
+    def __init__(self, wl, device, kv_loader=0, cascade="shared", layout="nhd",
+                 graph=False):
         import torch
         import paged_kv_decode_plan_gb300 as pkd
         self.torch = torch
@@ -271,6 +276,17 @@ class Runner:
         self.done = [None, None]
         self.turn = 0
         self.launches_per_step = 0
+        self.use_graph = graph
+        self.eager_steps = 0
+        self.graphs = {}
+        # timing events inside a graph must be real event-record nodes
+        # ("external"); without that option the timed pass runs eagerly
+        try:
+            self.timing_events = tuple(torch.cuda.Event(enable_timing=True, external=True)
+                                       for _ in range(4))
+        except TypeError:
+            self.timing_events = None
+        self.timings = []   # (decode_ms, prefix_ms) of timed graph steps
 
     def step(self, events=None):
         torch = self.torch
@@ -290,8 +306,42 @@ class Runner:
         ready = torch.cuda.Event()
         ready.record(self.copy_stream)
         main.wait_event(ready)
+        timed_in_graph = events is None or self.timing_events is not None
+        if self.use_graph and self.eager_steps >= 2 and timed_in_graph:
+            if not self.graphs:
+                self._capture()
+            self.graphs[(i, events is not None)].replay()
+            if events is not None:
+                torch.cuda.synchronize()
+                e = self.timing_events
+                self.timings.append((e[0].elapsed_time(e[1]),
+                                     e[2].elapsed_time(e[3]) if self.prefix else None))
+        else:
+            self._launch(i, events)
+            self.eager_steps += 1
+        done = torch.cuda.Event()
+        done.record(main)
+        self.done[i] = done
+
+    def _capture(self):
+        """One graph per workspace, plain and with timing events."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        for i in (0, 1):
+            for timed in ((False, True) if self.timing_events is not None else (False,)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    self._launch(i, self.timing_events if timed else None)
+                self.graphs[(i, timed)] = g
+        torch.cuda.synchronize()
+
+    def _launch(self, i, events=None):
+        """The kernel launches of one step on the current stream."""
+        torch = self.torch
+        main = torch.cuda.current_stream()
         launches = 0
         if self.prefix is not None:
+            pre = self.prefix
             if events is not None:
                 events[2].record(main)
             pre["ws"][i].run(pre["plan"], self.q, self.k, self.v, self.wl.sm_scale,
@@ -309,17 +359,24 @@ class Runner:
                 events[1].record(main)
             ws.run(plan, self.q, self.k, self.v, *part["dev"], self.wl.sm_scale,
                    out=part["out"], lse=part["lse"], phase="merge")
-            launches += 1 + (plan.num_split_requests > 0)
+            launches += 1 + (plan.num_split_requests > 0 or self.use_graph)
         if len(self.parts) == 2 or self.prefix is not None:
             a = self.parts[0] if self.prefix is None else self.prefix
             b = self.parts[-1]
             self.pkd.merge_states(a["out"], a["lse"], b["out"], b["lse"],
                                   v_out=self.final[0], s_out=self.final[1])
             launches += 1
-        done = torch.cuda.Event()
-        done.record(main)
-        self.done[i] = done
         self.launches_per_step = launches
+
+    def read_timings(self, events):
+        """(decode ms list, prefix ms list or None) of the timed pass."""
+        if self.timings:
+            dec = [t[0] for t in self.timings]
+            pre = [t[1] for t in self.timings] if self.prefix is not None else None
+            return dec, pre
+        dec = [e[0].elapsed_time(e[1]) for e in events]
+        pre = [e[2].elapsed_time(e[3]) for e in events] if self.prefix is not None else None
+        return dec, pre
 
     def result(self):
         if len(self.parts) == 2 or self.prefix is not None:
@@ -366,7 +423,7 @@ def run_ours(args, ranks):
     device = torch.device("cuda", ranks.local)
     wl = make_workload(args)
     runner = Runner(wl, device, kv_loader={"auto": 0, "tma": 1, "bulk": 2}[args.loader],
-                    cascade=args.cascade, layout=args.layout)
+                    cascade=args.cascade, layout=args.layout, graph=args.graph == "on")
     stream = torch.cuda.current_stream()
 
     # host plan time (median of 20)
@@ -381,6 +438,9 @@ def run_ours(args, ranks):
 
     for _ in range(args.warmup):
         runner.step()
+    if runner.use_graph:   # capture (after >= 2 eager steps) and replay before timing
+        for _ in range(3):
+            runner.step()
     torch.cuda.synchronize()
     status = runner.status()
     if status:
@@ -417,9 +477,7 @@ def run_ours(args, ranks):
         # end to end through the public API with host buffers
         e2e = run_e2e(args, runner, device, ranks)
         clocks.mark(1)
-    decode_ms = [e[0].elapsed_time(e[1]) for e in events]
-    prefix_ms = ([e[2].elapsed_time(e[3]) for e in events]
-                 if runner.prefix is not None else None)
+    decode_ms, prefix_ms = runner.read_timings(events)
     agg = aggregate(ranks, runner.kv_bytes(), elapsed, k)
     decode_mean_ms = ranks.reduce_max(statistics.fmean(decode_ms))
 
@@ -450,9 +508,11 @@ def run_ours(args, ranks):
         "cascade": (args.cascade if wl.name == "cascade" else None),
         "prefix_us": (round(statistics.fmean(prefix_ms) * 1e3, 2)
                       if prefix_ms else None),
+        "launch": "graph" if runner.use_graph else "eager",
         "timing": "pass 1 (value, ms_per_step): K steps between two events; pass 2 "
                   "(decode_us, roofline): the same K steps with events around each "
-                  "decode launch",
+                  "decode launch" + (" (inside the replayed graph, one step at a "
+                                     "time)" if runner.use_graph else ""),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel",
                      "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
@@ -635,6 +695,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", choices=["on", "off"], default="on",
+                    help="replay each step's launches as a CUDA graph (planning "
+                         "stays per step on the host)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -23,11 +23,11 @@ constexpr int kMergeThreads = 32 * kMergeWarps;
 
 // Folds partial states s0, s0 + stride, ... (< s1) of query head h into a
 // running (m, ws, acc) by the online rule: a new maximum rescales what was
-// folded so far; four states' loads are in flight per step.
+// folded so far; kUnroll states' loads are in flight per step.
+template <int kUnroll = 4>
 __device__ __forceinline__ void fold_states(const float *partials, long long slot_floats,
                                             int hq, int h, int s0, int s1, int stride,
                                             int lane, float &m, float &ws, float4 &acc) {
-  constexpr int kUnroll = 4;
   for (int j = s0; j < s1; j += kUnroll * stride) {
     float sv[kUnroll];
     float4 ov[kUnroll];
@@ -93,8 +93,9 @@ __global__ void __launch_bounds__(kMergeThreads)
     const int b = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
     float m = -INFINITY, ws = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    fold_states(partials, slot_floats, hq, h, b * chunks, (b + 1) * chunks, 1, lane, m,
-                ws, acc);
+    // a request's chunks are read in one round (the partials sit in L2)
+    fold_states<8>(partials, slot_floats, hq, h, b * chunks, (b + 1) * chunks, 1, lane, m,
+                   ws, acc);
     write_state<T>(out, lse, b, hq, h, lane, m, ws, acc);
   }
 }
