@@ -300,17 +300,20 @@ pkd_status pkd_append_kv(const pkd_problem *problem, const void *k_new,
  * the prefix tokens only; pkd_merge_states with the requests' suffix states
  * (pkd_run on their own pages) gives attention over prefix + suffix.
  * Per key/value head the prefix work is one dense tile (batch x g query rows
- * against the prefix), computed once, so the prefix is read once per
- * (head, 128-row tile, chunk) instead of once per request.
+ * against the prefix), computed once on the tensor cores, so the prefix is
+ * read once per (head, 256-row tile, chunk) instead of once per request.
  * Needs page_size % 16 == 0 (TMA boxes of 16 tokens) and a nonzero
  * problem->num_ctas-derived chunk count; other fields as for pkd_plan.
+ * A run captured in a CUDA graph stays valid while the prefix plan (length,
+ * chunks, row tiles) is unchanged; the kernel checks the image against its
+ * launch and reports a mismatch as PKD_DEVICE_BAD_PLAN.
  */
 typedef struct {
   pkd_problem problem;          /* resolved copy (num_ctas set) */
   int32_t prefix_len;           /* tokens of the shared prefix */
   int32_t prefix_num_pages;
   int32_t chunks;               /* KV chunks of the prefix (partial states per row) */
-  int32_t chunk_tiles;          /* 64-token tiles per chunk */
+  int32_t chunk_tiles;          /* 128-token tiles per chunk */
   int32_t row_tiles;            /* 256-row tiles per key/value head */
   int32_t num_blocks;           /* CTAs of the prefix kernel */
   int64_t int_ws_bytes_used;    /* bytes of the prefix plan image */
@@ -338,7 +341,8 @@ pkd_status pkd_plan_shared_prefix(const pkd_problem *problem,
                                   size_t int_ws_bytes, void *stream);
 
 /* Launches the shared-prefix kernel and the merge of its chunk states.
- * q [batch][Hq][D], k_pages / v_pages NHD; out [batch][Hq][D], lse [batch][Hq].
+ * q [batch][Hq][D], k_pages / v_pages in problem->kv_layout (NHD or HND);
+ * out [batch][Hq][D], lse [batch][Hq].
  * Range-check failures and wait timeouts land in the image's status word
  * (pkd_check_status on int_ws_dev). */
 pkd_status pkd_run_shared_prefix(const pkd_prefix_plan_t *plan, const void *q,
