@@ -528,25 +528,38 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages;
 
-  // the image must be the one the host planned for this launch
+  // The plan header and this CTA's [u_begin, u_end) come in one round trip,
+  // read by one warp (a lane per word) rather than by every thread of every
+  // CTA at once; the rest of the CTA takes them from shared memory.
+  __shared__ int32_t hdr[kHeaderWords + 2];
   const int32_t *img = p.image;
-  const int num_ctas = img[kHNumCtas];
-  const int num_units = img[kHNumUnits];
-  const int num_partials = img[kHNumPartials];
-  if (img[kHMagic] != kMagic || img[kHVersion] != kLayoutVersion ||
-      img[kHBatch] < 0 || img[kHBatch] > p.batch || img[kHTileTokens] != kTile ||
-      img[kHNumQoHeads] != p.hq || img[kHPageSize] != p.page_size ||
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    if (lane < kHeaderWords) {
+      hdr[lane] = __ldg(img + lane);
+    } else if (lane < kHeaderWords + 2) {
+      const long long w = kHeaderWords + static_cast<long long>(blockIdx.x) + (lane - kHeaderWords);
+      hdr[lane] = w < p.image_words ? __ldg(img + w) : -1;
+    }
+  }
+  __syncthreads();
+  // the image must be the one the host planned for this launch
+  const int num_ctas = hdr[kHNumCtas];
+  const int num_units = hdr[kHNumUnits];
+  const int num_partials = hdr[kHNumPartials];
+  if (hdr[kHMagic] != kMagic || hdr[kHVersion] != kLayoutVersion ||
+      hdr[kHBatch] < 0 || hdr[kHBatch] > p.batch || hdr[kHTileTokens] != kTile ||
+      hdr[kHNumQoHeads] != p.hq || hdr[kHPageSize] != p.page_size ||
       num_ctas != p.grid || num_units < 0 || num_partials < 0 ||
-      num_partials > p.max_partials || img[kHNumSplit] < 0 ||
-      image_offsets(num_ctas, num_units, img[kHNumSplit]).end > p.image_words) {
+      num_partials > p.max_partials || hdr[kHNumSplit] < 0 ||
+      image_offsets(num_ctas, num_units, hdr[kHNumSplit]).end > p.image_words) {
     if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
     return;
   }
-  const int32_t *cta_ptr = img + kHeaderWords;
-  const int32_t *units = cta_ptr + num_ctas + 1;
-  const int u_begin = cta_ptr[blockIdx.x], u_end = cta_ptr[blockIdx.x + 1];
+  const int32_t *units = img + kHeaderWords + num_ctas + 1;
+  const int u_begin = hdr[kHeaderWords], u_end = hdr[kHeaderWords + 1];
   Params q = p;
-  q.batch = img[kHBatch];  // this plan's batch (p.batch is the buffers' capacity)
+  q.batch = hdr[kHBatch];  // this plan's batch (p.batch is the buffers' capacity)
   if (u_begin < 0 || u_end > num_units || u_begin > u_end) {
     if (threadIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
     return;
