@@ -132,10 +132,22 @@ pkd_status plan_host_impl(const pkd_problem &in, const int32_t *kv_indptr,
     total_tokens += length[b];
   }
   if (kv_indices) {
-    for (int64_t i = kv_indptr[0]; i < kv_indptr[B]; ++i)
-      if (kv_indices[i] < 0 || kv_indices[i] >= p.num_pages)
-        return fail(PKD_ERR_PAGE_TABLE,
-                    "page id out of range at kv_indices[" + std::to_string(i) + "]");
+    // branch-free min / max pass (vectorised); the failing index is looked up
+    // only when a page id is out of range
+    const int64_t i0 = kv_indptr[0], i1 = kv_indptr[B];
+    const int32_t *__restrict ids = kv_indices + i0;
+    const int64_t n = i1 - i0;
+    int32_t lo = n > 0 ? ids[0] : 0, hi = lo;
+    for (int64_t i = 0; i < n; ++i) {
+      const int32_t v = ids[i];
+      lo = v < lo ? v : lo;
+      hi = v > hi ? v : hi;
+    }
+    if (n > 0 && (lo < 0 || hi >= p.num_pages))
+      for (int64_t i = i0; i < i1; ++i)
+        if (kv_indices[i] < 0 || kv_indices[i] >= p.num_pages)
+          return fail(PKD_ERR_PAGE_TABLE,
+                      "page id out of range at kv_indices[" + std::to_string(i) + "]");
   } else if (total_tokens > 0 && p.num_pages <= 0) {
     return fail(PKD_ERR_PAGE_TABLE, "non-empty table over an empty pool");
   }
