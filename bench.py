@@ -399,6 +399,28 @@ class Runner:
             return (prefix_tokens + int(wl.extra_tables["suffix"].lengths().sum())) * per_token
         return int(wl.table.lengths().sum()) * per_token
 
+    def total_bytes(self):
+        """All algorithmic bytes a step moves: KV (shared prefix once), the
+        queries read and outputs / lse written by every run, page indices, and
+        the fp32 partial states written and read back by the merges."""
+        wl = self.wl
+        elem = wl.k_pages.element_size()
+        rows = wl.batch * wl.num_qo_heads
+        slot = 4 * (wl.num_qo_heads * wl.head_dim + (wl.num_qo_heads + 3) // 4 * 4)
+        state = rows * (wl.head_dim * elem + 4)          # out + lse of one run
+        total = self.kv_bytes()
+        for part in self.parts:
+            total += 4 * int(part["table"].kv_indices.size)
+            total += rows * wl.head_dim * elem + state + 2 * part["plan"].num_partials * slot
+        if self.prefix is not None:
+            pre = self.prefix
+            total += 4 * int(pre["pages"].size)
+            total += rows * wl.head_dim * elem + state
+            total += 2 * wl.batch * pre["plan"].chunks * slot
+        if len(self.parts) == 2 or self.prefix is not None:
+            total += 3 * state                             # merge_states: two in, one out
+        return total
+
     def decode_kv_bytes(self):
         """KV bytes the timed decode launch reads (first table)."""
         wl = self.wl
@@ -498,6 +520,9 @@ def run_ours(args, ranks):
                    else "KV fits in L2: warm-L2 number",
                    "parallelism": "replicas (weak scaling, no collective)"},
         "us_per_batch": round(agg["ms_per_step"] * 1e3, 2),
+        "total_bytes_per_step": runner.total_bytes(),
+        "total_gbs": round(runner.total_bytes() * ranks.world / (agg["ms_per_step"] * 1e-3)
+                           / 1e9, 2),
         "hbm_frac_of_%s" % peak_kind: round(agg["value_gbs"] / ranks.world / peak, 4),
         "decode_us": round(decode_mean_ms * 1e3, 2),
         "plan_host_us": round(statistics.median(plan_times) * 1e6, 1),
