@@ -218,6 +218,9 @@ class Runner:
     With ``graph``, the kernel launches of a step are one CUDA graph per
     workspace (captured after the eager warm-up, valid for every later plan of
     the same capacity); planning and the plan copies stay on the host per step.
+    Queries, device page tables and outputs are also kept per workspace turn,
+    so a step's input copies and the previous step's read-back can overlap the
+    running step (the end-to-end loop).
     """
 
     def __init__(self, wl, device, kv_loader=0, cascade="shared", layout="nhd",
@@ -229,6 +232,7 @@ class Runner:
         self.wl = wl
         self.device = device
         self.q = wl.q.to(device)
+        self.qs = [self.q, self.q.clone()]
         self.k = wl.k_pages.to(device)
         self.v = wl.v_pages.to(device)
         self.layout = pkd.LAYOUT_HND if layout == "hnd" else pkd.LAYOUT_NHD
@@ -255,8 +259,9 @@ class Runner:
             self.prefix = dict(
                 pages=pages, last=int(pt.kv_last_page_len[0]),
                 ws=[pkd.PrefixWorkspace(prob, pages.size, device=device) for _ in range(2)],
-                out=torch.empty_like(self.q),
-                lse=torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
+                outs=[(torch.empty_like(self.q),
+                       torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
+                      for _ in range(2)])
         self.parts = []
         for t in self.tables:
             prob = pkd.make_problem(batch=t.batch, num_qo_heads=wl.num_qo_heads,
@@ -265,15 +270,24 @@ class Runner:
                                     min_chunks_per_request=wl.min_chunks_per_request,
                                     kv_loader=kv_loader, kv_layout=self.layout)
             ws = [pkd.Workspace(prob, device=device) for _ in range(2)]
-            dev = tuple(torch.from_numpy(a).to(device) for a in
-                        (t.kv_indptr, t.kv_indices, t.kv_last_page_len))
-            out = torch.empty_like(self.q)
-            lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
-            self.parts.append(dict(table=t, ws=ws, dev=dev, out=out, lse=lse))
-        self.final = (torch.empty_like(self.q),
-                      torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
+            # the three page-table arrays packed in one buffer per turn (one
+            # host-to-device copy per step); the API gets views into it
+            packed = pack_table(t)
+            n0, n1 = t.kv_indptr.size, t.kv_indices.size
+            packs = [torch.from_numpy(packed).to(device) for _ in range(2)]
+            devs = [(pk[:n0], pk[n0:n0 + n1], pk[n0 + n1:]) for pk in packs]
+            outs = [(torch.empty_like(self.q),
+                     torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
+                    for _ in range(2)]
+            self.parts.append(dict(table=t, ws=ws, devs=devs, packs=packs, outs=outs))
+        self.finals = [(torch.empty_like(self.q),
+                        torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
+                       for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(device)
+        self.read_stream = torch.cuda.Stream(device)
         self.done = [None, None]
+        self.read = [None, None]   # read-back of a turn's outputs (end to end)
+        self.last_turn = 0
         self.turn = 0
         self.launches_per_step = 0
         self.use_graph = graph
@@ -288,13 +302,23 @@ class Runner:
             self.timing_events = None
         self.timings = []   # (decode_ms, prefix_ms) of timed graph steps
 
-    def step(self, events=None):
+    def step(self, events=None, inputs=None, outputs=None):
+        """One step on workspace turn i.  ``inputs`` = (pinned q, pinned packed
+        page table per part) are copied in on the copy stream; ``outputs`` =
+        pinned (out, lse) receive the step's result on the read-back stream."""
         torch = self.torch
         main = torch.cuda.current_stream()
         i = self.turn
         self.turn ^= 1
+        self.last_turn = i
         if self.done[i] is not None:
             self.copy_stream.wait_event(self.done[i])
+        if inputs is not None:
+            q_h, tables_h = inputs
+            with torch.cuda.stream(self.copy_stream):
+                self.qs[i].copy_(q_h, non_blocking=True)
+                for part, th in zip(self.parts, tables_h):
+                    part["packs"][i].copy_(th, non_blocking=True)
         for part in self.parts:
             t = part["table"]
             part["plan"] = part["ws"][i].plan(t.kv_indptr, t.kv_last_page_len, None,
@@ -306,6 +330,8 @@ class Runner:
         ready = torch.cuda.Event()
         ready.record(self.copy_stream)
         main.wait_event(ready)
+        if self.read[i] is not None:   # this turn's previous outputs were read back
+            main.wait_event(self.read[i])
         timed_in_graph = events is None or self.timing_events is not None
         if self.use_graph and self.eager_steps >= 2 and timed_in_graph:
             if not self.graphs:
@@ -322,6 +348,15 @@ class Runner:
         done = torch.cuda.Event()
         done.record(main)
         self.done[i] = done
+        if outputs is not None:
+            res = self.result()
+            self.read_stream.wait_event(done)
+            with torch.cuda.stream(self.read_stream):
+                outputs[0].copy_(res[0], non_blocking=True)
+                outputs[1].copy_(res[1], non_blocking=True)
+            rd = torch.cuda.Event()
+            rd.record(self.read_stream)
+            self.read[i] = rd
 
     def _capture(self):
         """One graph per workspace, plain and with timing events."""
@@ -344,8 +379,8 @@ class Runner:
             pre = self.prefix
             if events is not None:
                 events[2].record(main)
-            pre["ws"][i].run(pre["plan"], self.q, self.k, self.v, self.wl.sm_scale,
-                             out=pre["out"], lse=pre["lse"])
+            pre["ws"][i].run(pre["plan"], self.qs[i], self.k, self.v, self.wl.sm_scale,
+                             out=pre["outs"][i][0], lse=pre["outs"][i][1])
             if events is not None:
                 events[3].record(main)
             launches += 2
@@ -353,18 +388,18 @@ class Runner:
             ws, plan = part["ws"][i], part["plan"]
             if events is not None and n == 0:
                 events[0].record(main)
-            ws.run(plan, self.q, self.k, self.v, *part["dev"], self.wl.sm_scale,
-                   out=part["out"], lse=part["lse"], phase="decode")
+            ws.run(plan, self.qs[i], self.k, self.v, *part["devs"][i], self.wl.sm_scale,
+                   out=part["outs"][i][0], lse=part["outs"][i][1], phase="decode")
             if events is not None and n == 0:
                 events[1].record(main)
-            ws.run(plan, self.q, self.k, self.v, *part["dev"], self.wl.sm_scale,
-                   out=part["out"], lse=part["lse"], phase="merge")
+            ws.run(plan, self.qs[i], self.k, self.v, *part["devs"][i], self.wl.sm_scale,
+                   out=part["outs"][i][0], lse=part["outs"][i][1], phase="merge")
             launches += 1 + (plan.num_split_requests > 0 or self.use_graph)
         if len(self.parts) == 2 or self.prefix is not None:
-            a = self.parts[0] if self.prefix is None else self.prefix
-            b = self.parts[-1]
-            self.pkd.merge_states(a["out"], a["lse"], b["out"], b["lse"],
-                                  v_out=self.final[0], s_out=self.final[1])
+            a = (self.parts[0] if self.prefix is None else self.prefix)["outs"][i]
+            b = self.parts[-1]["outs"][i]
+            self.pkd.merge_states(a[0], a[1], b[0], b[1],
+                                  v_out=self.finals[i][0], s_out=self.finals[i][1])
             launches += 1
         self.launches_per_step = launches
 
@@ -379,9 +414,11 @@ class Runner:
         return dec, pre
 
     def result(self):
+        """(out, lse) of the last step."""
+        i = self.last_turn
         if len(self.parts) == 2 or self.prefix is not None:
-            return self.final
-        return self.parts[0]["out"], self.parts[0]["lse"]
+            return self.finals[i]
+        return self.parts[0]["outs"][i]
 
     def status(self):
         words = [self.pkd.check_status(ws.int_ws) for p in self.parts for ws in p["ws"]]
@@ -426,6 +463,11 @@ class Runner:
         wl = self.wl
         per_token = 2 * wl.num_kv_heads * wl.head_dim * wl.k_pages.element_size()
         return int(self.tables[0].lengths().sum()) * per_token
+
+
+def pack_table(t):
+    """indptr, indices and last_page_len of a page table in one int32 array."""
+    return np.concatenate([t.kv_indptr, t.kv_indices, t.kv_last_page_len]).astype(np.int32)
 
 
 def make_workload(args):
@@ -565,22 +607,19 @@ def _explicit(problem, runner):
 def run_e2e(args, runner, device, ranks):
     """Same metric through the public API: every step copies its inputs
     (queries and page table) host-to-device from pinned memory, plans, runs,
-    and copies out and lse device-to-host into one of two pinned buffers; a
-    buffer is reused only after its copy has completed (the host does not
-    wait for each step, as a serving loop that overlaps steps would not), and
-    the timed region ends with a synchronise after the last read-back."""
+    and copies out and lse device-to-host into one of two pinned buffers.
+    The copies run on their own streams and overlap the neighbouring steps'
+    kernels (each turn's device buffers are reused only after their read-back
+    completed), as a serving loop would overlap them; the timed region ends
+    with a synchronise after the last read-back."""
     import torch
     wl = runner.wl
     q_h = wl.q.pin_memory()
-    tables_h = [tuple(torch.from_numpy(a).pin_memory() for a in
-                      (p["table"].kv_indptr, p["table"].kv_indices,
-                       p["table"].kv_last_page_len)) for p in runner.parts]
+    tables_h = [torch.from_numpy(pack_table(p["table"])).pin_memory() for p in runner.parts]
     outs_h = [(torch.empty(runner.q.shape, dtype=runner.q.dtype, pin_memory=True),
                torch.empty(runner.q.shape[:2], dtype=torch.float32, pin_memory=True))
               for _ in range(2)]
-    read = [None, None]
-    h2d = q_h.numel() * q_h.element_size() + sum(
-        sum(t.numel() * 4 for t in th) for th in tables_h)
+    h2d = q_h.numel() * q_h.element_size() + sum(th.numel() * 4 for th in tables_h)
     d2h = outs_h[0][0].numel() * outs_h[0][0].element_size() + outs_h[0][1].numel() * 4
     steps = max(3, min(args.steps, args.e2e_steps))
     turn = [0]
@@ -588,19 +627,7 @@ def run_e2e(args, runner, device, ranks):
     def one():
         i = turn[0]
         turn[0] ^= 1
-        if read[i] is not None:
-            read[i].synchronize()   # this buffer's previous read-back is done
-        runner.q.copy_(q_h, non_blocking=True)
-        for part, th in zip(runner.parts, tables_h):
-            for dst, src in zip(part["dev"], th):
-                dst.copy_(src, non_blocking=True)
-        runner.step()
-        res = runner.result()
-        outs_h[i][0].copy_(res[0], non_blocking=True)
-        outs_h[i][1].copy_(res[1], non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(torch.cuda.current_stream())
-        read[i] = ev
+        runner.step(inputs=(q_h, tables_h), outputs=outs_h[i])
 
     for _ in range(3):
         one()
