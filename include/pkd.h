@@ -313,7 +313,7 @@ typedef struct {
   int32_t prefix_len;           /* tokens of the shared prefix */
   int32_t prefix_num_pages;
   int32_t chunks;               /* KV chunks of the prefix (partial states per row) */
-  int32_t chunk_tiles;          /* 128-token tiles per chunk */
+  int32_t chunk_tiles;          /* 64-token tiles per chunk */
   int32_t row_tiles;            /* 256-row tiles per key/value head */
   int32_t num_blocks;           /* CTAs of the prefix kernel */
   int64_t int_ws_bytes_used;    /* bytes of the prefix plan image */

@@ -261,7 +261,7 @@ pkd_status plan_host_impl(const pkd_problem &in, const int32_t *kv_indptr,
 // chunks so that (heads x row tiles x chunks) fills the CTA budget, write the
 // image (header + page ids).
 namespace {
-constexpr int kPrefixTile = 128;  // tokens per prefix stage (prefix.cu)
+constexpr int kPrefixTile = 64;   // tokens per prefix stage (prefix.cu)
 constexpr int kPrefixRows = 256;  // query rows per prefix CTA: two 128-row MMA tiles (prefix.cu)
 }  // namespace
 

@@ -13,27 +13,28 @@
 // 128-row query tiles that share every K/V stage (loaded once for 256 rows):
 //   warps 0-3  softmax of query tile 0, thread r owns row r = tensor lane r
 //   warps 4-7  softmax of query tile 1
-//   warp 8     tensor-memory allocation; one thread issues tile 0's MMAs
-//   warp 9     one thread issues tile 1's MMAs (a thread can issue a
-//              tcgen05.mma only every ~120 cycles, so two issuers keep the
-//              tensor pipe fed with M 128 x N 128 MMAs)
-//   warps 10, 11  loaders of K and of V: TMA tiled loads of head h, 128-token
+//   warps 8, 9 one thread each issues the S = Q K^T MMAs of tile 0 / tile 1;
+//              warp 8 also allocates tensor memory
+//   warps 10, 11  one thread each issues the O += P V MMAs of tile 0 / 1 (an
+//              issuing thread spends ~80 cycles per tcgen05.mma and ~200 per
+//              barrier wait, so each chain gets its own thread)
+//   warps 12, 13  loaders of K and of V: TMA tiled loads of head h, 64-token
 //              stages, 16-token boxes, 128-byte swizzle; the prefix's ragged
 //              last box is copied with plain loads, zeros past the end.  K and
 //              V have their own full / empty barriers: K of a stage is free
 //              once both S MMAs have read it, well before P V frees V.
-// Per query tile q and 128-token tile i:
-//   S    = Q_q K_i^T             M 128, N 128, K 128 (A, B from shared memory)
-//   P    = exp2(S * c - ref)     softmax threads; P (f16 / bf16 pairs) is
+// Per query tile q and 64-token tile i (S double-buffered in tensor memory):
+//   S[i&1] = Q_q K_i^T           M 128, N 64, K 128 (A, B from shared memory)
+//   P      = exp2(S * c - ref)   softmax threads; P (f16 / bf16 pairs) is
 //                                stored over the S columns it came from
-//   O   += P V_i                 M 128, N 128, K 128 (A = P from tensor memory)
+//   O     += P V_i               M 128, N 128, K 64 (A = P from tensor memory)
 // bf16 P is split as hi + lo (two MMAs into the same accumulators).  The row
 // sum l is kept in fp32 registers.  The running reference moves only when a
-// row maximum grows by > 2^8; then O and l are rescaled.  S_q of tile i + 1
-// reuses P_q's columns, so the MMA thread issues it once P_q V_i has
-// completed; the two query tiles ping-pong, so while one warpgroup computes
-// exponentials the tensor core runs the other's MMAs.  N = 128 per MMA keeps
-// the tensor pipe's shared-memory reads per flop at the level it sustains.
+// row maximum grows by > 2^8; then O and l are rescaled (after P V of the
+// previous tile has completed).  With two S buffers the tensor core computes
+// S of tile i + 1 while the softmax works on tile i; S of tile i + 2 reuses
+// the columns of P_i and is issued once P_i V_i has completed.  Tensor memory
+// per query tile: 2 x 64 (S / P) + 128 (O) = 256 columns, 512 in all.
 // Each CTA writes fp32 partial states (o / l, lse) of its rows for its chunk
 // into slot b * chunks + c of the float workspace; a merge kernel folds the
 // chunks.
@@ -54,30 +55,30 @@ namespace {
 
 constexpr int kPQRows = 128;                       // rows per query tile (MMA M)
 constexpr int kPRows = 2 * kPQRows;                // query rows per CTA
-constexpr int kPTile = 128;                        // tokens per stage (MMA N of S)
-constexpr int kPHalfRegion = kPTile * 128;         // one 64-column block: 128 rows x 128 B
+constexpr int kPTile = 64;                         // tokens per stage (MMA N of S)
+constexpr int kPHalfRegion = kPTile * 128;         // one 64-column block: 64 rows x 128 B
 constexpr int kPTensorBytes = 2 * kPHalfRegion;    // K (or V) of one stage
 constexpr int kPOffV = kPTensorBytes;              // V after K in a stage
 constexpr int kPStageBytes = 2 * kPTensorBytes;
-constexpr int kPStages = 2;
+constexpr int kPStages = 4;
 constexpr int kPQBytes = kPQRows * 256;            // [d-half][row][128 B]
 constexpr int kSoftmaxThreads = 128;
-constexpr int kMmaWarp = 8, kLoadWarp = 10;  // warps 8, 9 issue MMAs; 10, 11 load
-constexpr int kPThreads = 32 * 12;
+constexpr int kMmaWarp = 8, kLoadWarp = 12;  // warps 8 .. 11 issue MMAs; 12, 13 load
+constexpr int kPThreads = 32 * 14;
 constexpr uint32_t kTmemCols = 512;
 
-// Tensor-memory columns of query tile q: S (128), then O (128).  P of token
-// half t (tokens 64 t .. 64 t + 63) is stored over S columns [64 t, 64 t + 64):
-// hi pairs in the first 32, bf16 lo pairs in the next 32.
-__host__ __device__ constexpr uint32_t col_s(int q) { return 256u * q; }
-__host__ __device__ constexpr uint32_t col_o(int q) { return 256u * q + kPTile; }
+// Tensor-memory columns of query tile q: two 64-column S buffers, then O
+// (128).  P of a tile is stored over its S buffer: hi pairs in the first 32
+// columns, bf16 lo pairs in the next 32.
+__host__ __device__ constexpr uint32_t col_s(int q, int b) { return 256u * q + 64u * b; }
+__host__ __device__ constexpr uint32_t col_o(int q) { return 256u * q + 128u; }
 static_assert(col_o(1) + kHeadDim <= kTmemCols, "tensor-memory budget");
 
 constexpr int kOffQ = kPStages * kPStageBytes;
 constexpr int kOffBars = kOffQ + 2 * kPQBytes;
-// full[tensor][S], empty[tensor][S], then per query tile s_full, p_full,
-// p_free, q_full, drain, and the ping-pong acknowledgement
-constexpr int kNumBars = 4 * kPStages + 11;
+// full[tensor][S], empty[tensor][S], then per query tile and S buffer
+// s_full, p_full, p_free, then per query tile q_full and the two drains
+constexpr int kNumBars = 4 * kPStages + 18;
 constexpr int kOffMisc = kOffBars + 8 * kNumBars;
 constexpr int kPSmem = 1024 + kOffMisc + 16;
 static_assert(kPSmem <= 227 * 1024, "shared memory budget");
@@ -100,12 +101,15 @@ struct Bars {
   // tensor 0 = K, 1 = V
   __device__ uint32_t full(int t, int s) const { return base + 8 * (t * kPStages + s); }
   __device__ uint32_t empty(int t, int s) const { return base + 8 * ((2 + t) * kPStages + s); }
-  __device__ uint32_t s_full(int q) const { return base + 8 * (4 * kPStages + q); }
-  __device__ uint32_t p_full(int q) const { return base + 8 * (4 * kPStages + 2 + q); }
-  __device__ uint32_t p_free(int q) const { return base + 8 * (4 * kPStages + 4 + q); }
-  __device__ uint32_t q_full(int q) const { return base + 8 * (4 * kPStages + 6 + q); }
-  __device__ uint32_t drain(int q) const { return base + 8 * (4 * kPStages + 8 + q); }
-  __device__ uint32_t ack() const { return base + 8 * (4 * kPStages + 10); }
+  // per query tile q and S buffer b (each completes once every two tiles)
+  __device__ uint32_t s_full(int q, int b) const { return base + 8 * (4 * kPStages + 2 * q + b); }
+  __device__ uint32_t p_full(int q, int b) const { return base + 8 * (4 * kPStages + 4 + 2 * q + b); }
+  __device__ uint32_t p_free(int q, int b) const { return base + 8 * (4 * kPStages + 8 + 2 * q + b); }
+  __device__ uint32_t q_full(int q) const { return base + 8 * (4 * kPStages + 12 + q); }
+  // completion of every MMA issued by the S (role 0) or P V (role 1) thread of tile q
+  __device__ uint32_t drain(int q, int role) const {
+    return base + 8 * (4 * kPStages + 14 + 2 * q + role);
+  }
 };
 
 __device__ __forceinline__ void give_up(const PrefixParams &p, volatile int *abort) {
@@ -141,7 +145,7 @@ __device__ __forceinline__ long long checked_page(const PrefixParams &p, const i
 }
 
 // Warp kLoadWarp + tensor: fills K (tensor 0) or V (tensor 1) of stage
-// it % S with tokens [128 t, 128 t + 128) of head h.
+// it % S with tokens [64 t, 64 t + 64) of head h.
 __device__ void load_prefix(const PrefixParams &p, const CUtensorMap *map, int tensor, int h,
                             int t_begin, int n, uint8_t *stages, const Bars &bars,
                             volatile int *abort) {
@@ -162,7 +166,7 @@ __device__ void load_prefix(const PrefixParams &p, const CUtensorMap *map, int t
     const int nfull = valid / kTile;
     uint8_t *dst_tile = stages + s * kPStageBytes + tensor * kPOffV;
     if (valid < kPTile) {
-      // rows [16 nfull, 128): plain copies up to the prefix end, zeros after
+      // rows [16 nfull, 64): plain copies up to the prefix end, zeros after
       const int first = nfull * kTile;
       const int items = (kPTile - first) * 16;  // rows x 16-byte chunks
       for (int idx = lane; idx < items; idx += 32) {
@@ -204,99 +208,108 @@ __device__ void load_prefix(const PrefixParams &p, const CUtensorMap *map, int t
   __syncwarp();
 }
 
-// Ping-pong: tile 1's S of KV tile i is issued only after tile 0's softmax of
-// tile i has finished (so the two softmaxes alternate with the other tile's
-// MMAs); its issuer acknowledges each such wait, and tile 0's S of tile i + 1
-// waits for that acknowledgement, so neither side can pass a barrier phase
-// the other has not observed yet.
+// Issuing threads of query tile q.  Tile i uses S buffer i & 1; the s_full /
+// p_full / p_free barriers of a buffer complete once per two tiles, so tile i
+// waits for their phase (i >> 1) & 1.  Neither thread can run two phases
+// ahead of a waiter: S of tile i + 2 needs P V of tile i, which needs P of
+// tile i.
+//
+// Warp kMmaWarp + q: S[i & 1] = Q_q K_i^T, eight K = 16 steps over the head
+// dim.  S of tile i overwrites P of tile i - 2, so it waits for P V of tile
+// i - 2 to complete (p_free).
 template <typename T>
-__device__ void issue_mmas(const PrefixParams &p, int n, int q, int nq, uint8_t *smem,
-                           uint32_t tmem, const Bars &bars, volatile int *abort) {
+__device__ void issue_qk(const PrefixParams &p, int n, int q, uint8_t *smem, uint32_t tmem,
+                         const Bars &bars, volatile int *abort) {
   constexpr bool kSplit = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t kIdescQK = tc::idesc_f16(kSplit, kPQRows, kPTile, false);
-  constexpr uint32_t kIdescPV = tc::idesc_f16(kSplit, kPQRows, kHeadDim, true);
   const uint32_t base = ptx::smem_u32(smem);
   // Descriptors are built once; a k-step adds its byte offset / 16 to the
   // start-address field (no carry: shared addresses stay below 256 KB).
   const uint64_t q_desc = tc::smem_desc_sw128(base + kOffQ + q * kPQBytes, 16, 1024);
   const uint64_t k_desc = tc::smem_desc_sw128(base, 16, 1024);
-  const uint64_t v_desc = tc::smem_desc_sw128(base + kPOffV, kPHalfRegion, 1024);
-  const uint32_t t_s = tmem + col_s(q), t_o = tmem + col_o(q);
-
-  // S_q = Q_q K_i^T: eight K = 16 steps over the head dim
-  auto issue_qk = [&](int i) -> bool {
-    if (q == 1) {
-      if (!wait_phase(bars.p_full(0), i & 1, abort)) return false;
-      ptx::mbar_arrive(bars.ack());
-    } else if (nq == 2 && i > 0) {
-      if (!wait_phase(bars.ack(), (i - 1) & 1, abort)) return false;
-    }
-    if (!wait_phase(bars.full(0, i % kPStages), (i / kPStages) & 1, abort)) return false;
+  bool ok = wait_phase(bars.q_full(q), 0, abort);
+  bool issued = false;
+  for (int i = 0; ok && i < n; ++i) {
+    const int b = i & 1;
+    if (i >= 2 && !(ok = wait_phase(bars.p_free(q, b), ((i - 2) >> 1) & 1, abort))) break;
+    if (!(ok = wait_phase(bars.full(0, i % kPStages), (i / kPStages) & 1, abort))) break;
     tc::fence_after_sync();
+    issued = true;
     const uint64_t kd = k_desc + (((i % kPStages) * kPStageBytes) >> 4);
+    const uint32_t t_s = tmem + col_s(q, b);
 #pragma unroll
     for (int kk = 0; kk < kHeadDim / 16; ++kk) {
       const uint32_t off = ((kk >> 2) * kPQRows * 128 + (kk & 3) * 32) >> 4;
       const uint32_t koff = ((kk >> 2) * kPHalfRegion + (kk & 3) * 32) >> 4;
       tc::mma_f16(t_s, q_desc + off, kd + koff, kIdescQK, kk > 0);
     }
-    tc::commit(bars.s_full(q));
+    tc::commit(bars.s_full(q, b));
     tc::commit(bars.empty(0, i % kPStages));  // one arrival per query tile
-    return true;
-  };
-
-  bool ok = wait_phase(bars.q_full(q), 0, abort);
-  bool issued = false;
-  if (ok) {
-    issued = true;
-    ok = issue_qk(0);
-  }
-  for (int i = 0; ok && i < n; ++i) {
-    // the softmax has read S_q and written P_q of tile i
-    if (!(ok = wait_phase(bars.p_full(q), i & 1, abort))) break;
-    if (!(ok = wait_phase(bars.full(1, i % kPStages), (i / kPStages) & 1, abort))) break;
-    tc::fence_after_sync();
-    // O += P V: k-steps of 16 tokens; V rows 16 j .. 16 j + 15 are two 8-row
-    // groups (SBO 1024), V's d-halves 16 KB apart (LBO); P of those tokens
-    // sits in S columns 64 (j / 4) + 8 (j % 4) (+ 32 for the lo copy)
-    const uint64_t vd = v_desc + (((i % kPStages) * kPStageBytes) >> 4);
-#pragma unroll
-    for (int j = 0; j < kPTile / 16; ++j) {
-      const uint32_t a = t_s + 64 * (j >> 2) + 8 * (j & 3);
-      tc::mma_f16_tmem_a(t_o, a, vd + ((j * 2048) >> 4), kIdescPV, i > 0 || j > 0);
-      if (kSplit) tc::mma_f16_tmem_a(t_o, a + 32, vd + ((j * 2048) >> 4), kIdescPV, true);
-    }
-    tc::commit(bars.p_free(q));
-    tc::commit(bars.empty(1, i % kPStages));  // one arrival per query tile
-    if (i + 1 < n) {
-      // S_q of tile i + 1 overwrites P_q: only once P_q V_i has completed
-      if (!(ok = wait_phase(bars.p_free(q), i & 1, abort))) break;
-      if (!(ok = issue_qk(i + 1))) break;
-    }
   }
   if (!ok) give_up(p, abort);
   if (issued) {
     // every MMA of this thread completes before tensor memory is released
-    tc::commit(bars.drain(q));
-    wait_phase(bars.drain(q), 0, abort, true);
+    tc::commit(bars.drain(q, 0));
+    wait_phase(bars.drain(q, 0), 0, abort, true);
   }
 }
 
-// One 128-token tile of one query row (warp-collective): row maximum, lazy
-// reference move (rescaling O and l when it moves and O holds earlier tiles),
-// P stored over S, row sum.  kFull: every token of the tile is in the prefix.
-template <typename T, bool kFull>
-__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int valid, float cs,
-                                             bool rescale_o, float &ref, float &l) {
+// Warp kMmaWarp + 2 + q: O += P_i V_i once the softmax has written P_i over
+// S[i & 1] (p_full); k-steps of 16 tokens, V rows 16 j .. 16 j + 15 are two
+// 8-row groups (SBO 1024), V's d-halves one half region apart (LBO).
+template <typename T>
+__device__ void issue_pv(const PrefixParams &p, int n, int q, uint8_t *smem, uint32_t tmem,
+                         const Bars &bars, volatile int *abort) {
   constexpr bool kSplit = std::is_same<T, __nv_bfloat16>::value;
+  constexpr uint32_t kIdescPV = tc::idesc_f16(kSplit, kPQRows, kHeadDim, true);
+  const uint64_t v_desc = tc::smem_desc_sw128(ptx::smem_u32(smem) + kPOffV, kPHalfRegion, 1024);
+  const uint32_t t_o = tmem + col_o(q);
+  bool ok = true, issued = false;
+  for (int i = 0; i < n; ++i) {
+    const int b = i & 1;
+    // V is normally resident long before P: wait for it first so the MMAs
+    // follow the P wait at once
+    if (!(ok = wait_phase(bars.full(1, i % kPStages), (i / kPStages) & 1, abort))) break;
+    if (!(ok = wait_phase(bars.p_full(q, b), (i >> 1) & 1, abort))) break;
+    tc::fence_after_sync();
+    issued = true;
+    const uint64_t vd = v_desc + (((i % kPStages) * kPStageBytes) >> 4);
+#pragma unroll
+    for (int j = 0; j < kPTile / 16; ++j) {
+      const uint32_t a = tmem + col_s(q, b) + 8 * j;
+      tc::mma_f16_tmem_a(t_o, a, vd + ((j * 2048) >> 4), kIdescPV, i > 0 || j > 0);
+      if (kSplit) tc::mma_f16_tmem_a(t_o, a + 32, vd + ((j * 2048) >> 4), kIdescPV, true);
+    }
+    tc::commit(bars.p_free(q, b));
+    tc::commit(bars.empty(1, i % kPStages));  // one arrival per query tile
+  }
+  if (!ok) give_up(p, abort);
+  if (issued) {
+    tc::commit(bars.drain(q, 1));
+    wait_phase(bars.drain(q, 1), 0, abort, true);
+  }
+}
+
+// One 64-token tile of one query row (warp-collective): row maximum, lazy
+// reference move, P stored over S, row sum.  When the reference moves and O
+// holds earlier tiles, O is rescaled once P V of the previous tile has
+// completed (barrier o_bar, parity o_par); false if that wait gave up.
+// kFull: every token of the tile is in the prefix.
+template <typename T, bool kFull>
+__device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_o, int valid, float cs,
+                                             bool rescale_o, uint32_t o_bar, uint32_t o_par,
+                                             volatile int *abort, float &ref, float &l) {
+  constexpr bool kSplit = std::is_same<T, __nv_bfloat16>::value;
+  float s[kPTile];
+  tc::ld64(t_s, s);
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if (kFull) {
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float s[64];
-    tc::ld64(t_s + 64 * half, s);
+    for (int j = 0; j < kPTile; j += 2) m4[(j >> 1) & 3] = ptx::fmax3(m4[(j >> 1) & 3], s[j], s[j + 1]);
+  } else {
 #pragma unroll
-    for (int j = 0; j < 64; ++j)
-      if (kFull || 64 * half + j < valid) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+    for (int j = 0; j < kPTile; ++j)
+      if (j < valid) m4[j & 3] = fmaxf(m4[j & 3], s[j]);
   }
   const float cand = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * cs;
   const bool need = cand > ref + kLazy;
@@ -308,6 +321,8 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int val
     }
     l *= alpha;
     if (rescale_o) {
+      if (!warp_wait(o_bar, o_par, abort)) return false;
+      tc::fence_after_sync();
 #pragma unroll 1
       for (int cc = 0; cc < kHeadDim / 16; ++cc) {
         float v[16];
@@ -319,35 +334,37 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int val
     }
   }
   const float rc = ref == -INFINITY ? 0.f : ref;  // clamp
-  float lsum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-  for (int half = 0; half < 2; ++half) {
-    // P of this token half replaces the S values it was computed from
-    // (the whole half is in registers before any of its columns is written)
-    float s[64];
-    tc::ld64(t_s + 64 * half, s);
+  const float2 cs2 = make_float2(cs, cs), nrc2 = make_float2(-rc, -rc);
+  float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  // 16 tokens (8 pairs, 8 tensor-memory columns of P) at a time, so few
+  // packed pairs are live; every S value is already in registers, so the
+  // bf16 lo pairs may overwrite S columns of later tokens
 #pragma unroll
-    for (int chunk = 0; chunk < 2; ++chunk) {
-      float hi[16], lo[16];  // packed pairs, carried as float bit patterns
+  for (int c8 = 0; c8 < kPTile / 16; ++c8) {
+    float hi[8], lo[8];  // packed pairs, carried as float bit patterns
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int k = 32 * chunk + 2 * j;
-        const int t = 64 * half + k;
-        const float e0 = kFull || t < valid ? ptx::ex2(fmaf(s[k], cs, -rc)) : 0.f;
-        const float e1 = kFull || t + 1 < valid ? ptx::ex2(fmaf(s[k + 1], cs, -rc)) : 0.f;
-        const uint32_t h2 = ptx::pack2<T>(e0, e1);
-        hi[j] = __uint_as_float(h2);
-        if (kSplit) {
-          const float2 f = ptx::unpack2<T>(h2);
-          lo[j] = __uint_as_float(ptx::pack2<T>(e0 - f.x, e1 - f.y));
-        }
-        lsum[j & 3] += e0 + e1;
+    for (int j = 0; j < 8; ++j) {
+      const int pair = 8 * c8 + j, k = 2 * pair;
+      const float2 x = ptx::ffma2(make_float2(s[k], s[k + 1]), cs2, nrc2);
+      float2 e = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+      if (!kFull) {
+        e.x = k < valid ? e.x : 0.f;
+        e.y = k + 1 < valid ? e.y : 0.f;
       }
-      tc::st16(t_s + 64 * half + 16 * chunk, hi);
-      if (kSplit) tc::st16(t_s + 64 * half + 32 + 16 * chunk, lo);
+      const uint32_t h2 = ptx::pack2<T>(e.x, e.y);
+      hi[j] = __uint_as_float(h2);
+      if (kSplit) {
+        const float2 r = ptx::fsub2(e, ptx::unpack2<T>(h2));
+        lo[j] = __uint_as_float(ptx::pack2<T>(r.x, r.y));
+      }
+      lsum[j & 1] = ptx::fadd2(lsum[j & 1], e);
     }
+    tc::st8(t_s + 8 * c8, hi);
+    if (kSplit) tc::st8(t_s + 32 + 8 * c8, lo);
   }
-  l += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+  const float2 ls = ptx::fadd2(lsum[0], lsum[1]);
+  l += ls.x + ls.y;
+  return true;
 }
 
 // Warps 4q .. 4q + 3: row r of query tile q (zeros past the last row) into
@@ -380,7 +397,6 @@ __device__ void softmax_rows(const PrefixParams &p, int q, int h, int rt, int c,
   const int r = threadIdx.x & (kSoftmaxThreads - 1);
   const int lane = r & 31;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
-  const uint32_t t_s = tmem + lane_base + col_s(q);
   const uint32_t t_o = tmem + lane_base + col_o(q);
   const int rows = p.batch * p.group;
   const int row_id = rt * kPRows + q * kPQRows + r;
@@ -393,21 +409,30 @@ __device__ void softmax_rows(const PrefixParams &p, int q, int h, int rt, int c,
   float l = 0.f;          // row sum of P
   bool failed = false;
   for (int i = 0; i < n; ++i) {
-    if (!warp_wait(bars.s_full(q), i & 1, abort)) {
+    const int sb = i & 1;
+    if (!warp_wait(bars.s_full(q, sb), (i >> 1) & 1, abort)) {
       failed = true;
       break;
     }
     tc::fence_after_sync();
-    // S_q of tile i was issued after P_q V_{i-1} completed, so O holds tiles
-    // < i from here on
+    // S of tile i may be ready before P V of tile i - 1 has completed (it was
+    // issued into the other buffer); a rescale of O waits for that P V, whose
+    // completion is phase ((i - 1) >> 1) & 1 of p_free of the other buffer
+    const uint32_t t_s = tmem + lane_base + col_s(q, sb);
+    const uint32_t o_bar = bars.p_free(q, sb ^ 1);
+    const uint32_t o_par = ((i - 1) >> 1) & 1;
     const int valid = min(kPTile, p.length - (t_begin + i) * kPTile);
-    if (valid == kPTile)
-      softmax_tile<T, true>(t_s, t_o, valid, cs, i > 0, ref, l);
-    else
-      softmax_tile<T, false>(t_s, t_o, valid, cs, i > 0, ref, l);
+    const bool ok =
+        valid == kPTile
+            ? softmax_tile<T, true>(t_s, t_o, valid, cs, i > 0, o_bar, o_par, abort, ref, l)
+            : softmax_tile<T, false>(t_s, t_o, valid, cs, i > 0, o_bar, o_par, abort, ref, l);
+    if (!ok) {
+      failed = true;
+      break;
+    }
     tc::wait_st();
     tc::fence_before_sync();
-    ptx::mbar_arrive(bars.p_full(q));
+    ptx::mbar_arrive(bars.p_full(q, sb));
   }
   if (failed) {
     if (lane == 0) give_up(p, abort);
@@ -425,7 +450,7 @@ __device__ void softmax_rows(const PrefixParams &p, int q, int h, int rt, int c,
     }
     return;
   }
-  if (!warp_wait(bars.p_free(q), (n - 1) & 1, abort)) {
+  if (!warp_wait(bars.p_free(q, (n - 1) & 1), ((n - 1) >> 1) & 1, abort)) {
     if (lane == 0) give_up(p, abort);
     return;
   }
@@ -487,13 +512,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
         ptx::mbar_init(bars.empty(t, s), nq);  // released by each live query tile
       }
     for (int q = 0; q < 2; ++q) {
-      ptx::mbar_init(bars.s_full(q), 1);
-      ptx::mbar_init(bars.p_full(q), kSoftmaxThreads);
-      ptx::mbar_init(bars.p_free(q), 1);
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(bars.s_full(q, b), 1);
+        ptx::mbar_init(bars.p_full(q, b), kSoftmaxThreads);
+        ptx::mbar_init(bars.p_free(q, b), 1);
+      }
       ptx::mbar_init(bars.q_full(q), p.q_tma ? 1 : kSoftmaxThreads);
-      ptx::mbar_init(bars.drain(q), 1);
+      ptx::mbar_init(bars.drain(q, 0), 1);
+      ptx::mbar_init(bars.drain(q, 1), 1);
     }
-    ptx::mbar_init(bars.ack(), 1);
     *abort = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async();
@@ -517,7 +544,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncwarp();
     load_prefix(p, tensor ? &map_v : &map_k, tensor, h, t_begin, n, smem, bars, abort);
   } else {
-    const int q = warp < kMmaWarp ? warp >> 2 : warp - kMmaWarp;
+    const int q = warp < kMmaWarp ? warp >> 2 : (warp - kMmaWarp) & 1;
     if (warp < kMmaWarp && q < nq && !p.q_tma) load_q(p, q, h, rt, smem, bars);
     if (warp == kMmaWarp) {
       tc::alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -531,8 +558,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (warp < kMmaWarp) {
       if (q < nq) softmax_rows<T>(p, q, h, rt, c, t_begin, n, smem, tmem, bars, abort);
     } else {
-      if ((threadIdx.x & 31) == 0 && n > 0 && q < nq)
-        issue_mmas<T>(p, n, q, nq, smem, tmem, bars, abort);
+      if ((threadIdx.x & 31) == 0 && n > 0 && q < nq) {
+        if (warp < kMmaWarp + 2)
+          issue_qk<T>(p, n, q, smem, tmem, bars, abort);
+        else
+          issue_pv<T>(p, n, q, smem, tmem, bars, abort);
+      }
       __syncwarp();
     }
   }
