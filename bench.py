@@ -223,7 +223,7 @@ class Runner:
     running step (the end-to-end loop).
     """
 
-    def __init__(self, wl, device, kv_loader=0, cascade="shared", layout="nhd",
+    def __init__(self, wl, device, kv_loader=0, cascade="fused", layout="nhd",
                  graph=False):
         import torch
         import paged_kv_decode_plan_gb300 as pkd
@@ -239,9 +239,13 @@ class Runner:
         if layout == "hnd":  # same values, [pages][Hkv][P][D]
             self.k = self.k.transpose(1, 2).contiguous()
             self.v = self.v.transpose(1, 2).contiguous()
-        # cascade: the shared prefix once through the shared-prefix kernel
-        # ("shared"), or listed in every request's table ("per-request")
-        self.shared = wl.name == "cascade" and cascade == "shared"
+        # cascade: the shared prefix once through the shared-prefix kernel,
+        # its chunk states folded into the suffix states by the cascade merge
+        # ("fused"), or merged to prefix states first and combined with
+        # merge_states ("shared"); or listed in every request's table
+        # ("per-request")
+        self.shared = wl.name == "cascade" and cascade in ("shared", "fused")
+        self.fused = wl.name == "cascade" and cascade == "fused"
         if wl.name == "cascade" and not self.shared:
             self.tables = [wl.extra_tables["prefix"], wl.extra_tables["suffix"]]
         elif self.shared:
@@ -375,6 +379,24 @@ class Runner:
         torch = self.torch
         main = torch.cuda.current_stream()
         launches = 0
+        if self.fused:
+            pre, part = self.prefix, self.parts[0]
+            ws, plan, final = part["ws"][i], part["plan"], self.finals[i]
+            if events is not None:
+                events[2].record(main)
+            pre["ws"][i].run_states(pre["plan"], self.qs[i], self.k, self.v,
+                                    self.wl.sm_scale)
+            if events is not None:
+                events[3].record(main)
+                events[0].record(main)
+            ws.run(plan, self.qs[i], self.k, self.v, *part["devs"][i], self.wl.sm_scale,
+                   out=final[0], lse=final[1], phase="decode")
+            if events is not None:
+                events[1].record(main)
+            self.pkd.run_cascade_merge(plan, pre["plan"], ws, pre["ws"][i], final[0],
+                                       final[1])
+            self.launches_per_step = 3
+            return
         if self.prefix is not None:
             pre = self.prefix
             if events is not None:
@@ -446,6 +468,15 @@ class Runner:
         slot = 4 * (wl.num_qo_heads * wl.head_dim + (wl.num_qo_heads + 3) // 4 * 4)
         state = rows * (wl.head_dim * elem + 4)          # out + lse of one run
         total = self.kv_bytes()
+        if self.fused:
+            pre, part = self.prefix, self.parts[0]
+            prefix_states = wl.batch * pre["plan"].chunks * slot
+            total += 4 * int(pre["pages"].size) + 4 * int(part["table"].kv_indices.size)
+            total += 2 * rows * wl.head_dim * elem          # q read by both kernels
+            total += state + 2 * part["plan"].num_partials * slot   # suffix decode
+            total += 2 * prefix_states                       # prefix states out and in
+            total += 2 * state                               # merge: suffix state in, final out
+            return total
         for part in self.parts:
             total += 4 * int(part["table"].kv_indices.size)
             total += rows * wl.head_dim * elem + state + 2 * part["plan"].num_partials * slot
@@ -752,9 +783,12 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--layout", choices=["nhd", "hnd"], default="nhd",
                     help="page tensor layout (the same values either way)")
-    ap.add_argument("--cascade", choices=["shared", "per-request"], default="shared",
-                    help="cascade workload: shared-prefix kernel, or the prefix "
-                         "pages listed in every request's table")
+    ap.add_argument("--cascade", choices=["fused", "shared", "per-request"],
+                    default="fused",
+                    help="cascade workload: shared-prefix kernel states folded into "
+                         "the suffix states by the cascade merge (fused), prefix "
+                         "states merged first and combined by merge_states (shared), "
+                         "or the prefix pages listed in every request's table")
     ap.add_argument("--batch", type=int, default=None,
                     help="smaller batch of the longctx / cascade workload (profiling)")
     ap.add_argument("--loader", choices=["auto", "tma", "bulk"], default="auto",

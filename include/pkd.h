@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define PKD_ABI_VERSION 2
+#define PKD_ABI_VERSION 3
 
 typedef enum {
   PKD_OK = 0,
@@ -350,6 +350,63 @@ pkd_status pkd_run_shared_prefix(const pkd_prefix_plan_t *plan, const void *q,
                                  void *int_ws_dev, void *float_ws_dev,
                                  size_t float_ws_bytes, float sm_scale, void *out,
                                  float *lse, void *stream);
+
+/* The shared-prefix kernel alone: leaves the state of every (request, query
+ * head, prefix chunk) in float_ws_dev (fp32, the layout of pkd_run's partial
+ * states, slot b * plan->chunks + c) for pkd_run_cascade_merge.  Arguments
+ * and errors as pkd_run_shared_prefix, without out / lse. */
+pkd_status pkd_run_shared_prefix_states(const pkd_prefix_plan_t *plan, const void *q,
+                                        const void *k_pages, const void *v_pages,
+                                        void *int_ws_dev, void *float_ws_dev,
+                                        size_t float_ws_bytes, float sm_scale,
+                                        void *stream);
+
+/*
+ * Cascade attention in one call ([W] "Attention states": the states of a
+ * shared prefix and of each request's own suffix merge into the state over
+ * both): attention of every request over the shared prefix followed by its
+ * suffix.  `plan` is the suffix plan (pkd_plan over each request's own
+ * pages; kv_* describe those pages) and `prefix_plan` the shared prefix
+ * (pkd_plan_shared_prefix); both must have the same batch, heads, head_dim,
+ * dtype, page_size, num_pages and kv_layout (else PKD_ERR_INVALID_ARG, no
+ * launch), and one q / k_pages / v_pages serves both.  Launches, on
+ * `stream`: the shared-prefix kernel (chunk states into
+ * prefix_float_ws_dev), the decode kernel of pkd_run_decode (unsplit rows'
+ * suffix states into out / lse, split rows' partial states into
+ * float_ws_dev), then pkd_run_cascade_merge.  out [batch][Hq][D] and lse
+ * [batch][Hq] receive the final states; a request with no tokens at all gets
+ * (0, -inf).  No separate prefix out / lse and no pkd_merge_states pass: the
+ * prefix states stay fp32 until the final merge.  Workspaces: each plan's
+ * own, as for pkd_run and pkd_run_shared_prefix.  Graph capture: as for
+ * pkd_run_shared_prefix (the prefix plan, which fixes the batch, must stay
+ * unchanged); the suffix plan may change between replays within the same
+ * batch.  Device-side mismatches land in the suffix image's status word
+ * (PKD_DEVICE_BAD_PLAN) or the prefix image's (pkd_check_status).
+ */
+pkd_status pkd_run_cascade(const pkd_plan_t *plan, const void *q, const void *k_pages,
+                           const void *v_pages, const int32_t *kv_indptr_d,
+                           const int32_t *kv_indices_d,
+                           const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                           void *float_ws_dev, size_t float_ws_bytes,
+                           const pkd_prefix_plan_t *prefix_plan, void *prefix_int_ws_dev,
+                           void *prefix_float_ws_dev, size_t prefix_float_ws_bytes,
+                           float sm_scale, void *out, float *lse, void *stream);
+
+/* The last launch of pkd_run_cascade, for callers that launch the prefix
+ * states (pkd_run_shared_prefix_states) and the suffix decode
+ * (pkd_run_decode into out / lse) themselves, in that order on `stream`,
+ * immediately before this call.  Per (request b, query head h) row it folds
+ * the prefix chunk states with the suffix state (the request's partial
+ * states if its suffix plan split it, else the out / lse row) and writes the
+ * result over out / lse.  Launched as a programmatic dependent of the decode
+ * kernel. */
+pkd_status pkd_run_cascade_merge(const pkd_plan_t *plan, void *int_ws_dev,
+                                 const void *float_ws_dev, size_t float_ws_bytes,
+                                 const pkd_prefix_plan_t *prefix_plan,
+                                 const void *prefix_int_ws_dev,
+                                 const void *prefix_float_ws_dev,
+                                 size_t prefix_float_ws_bytes, void *out, float *lse,
+                                 void *stream);
 
 #ifdef __cplusplus
 }

@@ -8,8 +8,10 @@ missing, every call raises; there is no other implementation to fall back to.
 
 Entry points (same names as the C ABI without the ``pkd_`` prefix):
 ``workspace_size``, ``plan_host``, ``plan``, ``run``, ``merge_states``,
-``check_status``, plus :class:`Workspace`, which allocates the buffers a
-capacity needs.
+``check_status``, the shared-prefix calls (``plan_shared_prefix``,
+``run_shared_prefix``, ``run_shared_prefix_states``, ``run_cascade``,
+``run_cascade_merge``), ``append_kv``, plus :class:`Workspace` and
+:class:`PrefixWorkspace`, which allocate the buffers a capacity needs.
 """
 from __future__ import annotations
 
@@ -29,12 +31,15 @@ STATUS_NAMES = {0: "PKD_OK", -1: "PKD_ERR_INVALID_ARG", -2: "PKD_ERR_PAGE_TABLE"
                 -3: "PKD_ERR_WORKSPACE", -4: "PKD_ERR_UNSUPPORTED",
                 -5: "PKD_ERR_CUDA", -6: "PKD_ERR_DEVICE_CHECK"}
 
+ABI_VERSION = 3  # PKD_ABI_VERSION of include/pkd.h
+
 # every symbol include/pkd.h declares
 EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
             "pkd_plan_host", "pkd_plan", "pkd_run", "pkd_run_decode",
             "pkd_run_merge", "pkd_merge_states", "pkd_check_status",
             "pkd_run_static", "pkd_prefix_workspace_size", "pkd_plan_shared_prefix",
-            "pkd_run_shared_prefix", "pkd_append_kv")
+            "pkd_run_shared_prefix", "pkd_append_kv", "pkd_run_shared_prefix_states",
+            "pkd_run_cascade", "pkd_run_cascade_merge")
 
 
 class PkdError(RuntimeError):
@@ -113,12 +118,18 @@ def load():
                                            vp, ctypes.c_size_t, vp, ctypes.c_size_t, vp]
     lib.pkd_run_shared_prefix.argtypes = [ctypes.POINTER(PrefixPlan), vp, vp, vp, vp, vp,
                                           ctypes.c_size_t, ctypes.c_float, vp, vp, vp]
-    for name in ("pkd_workspace_size", "pkd_plan_host", "pkd_plan", "pkd_run",
-                 "pkd_run_decode", "pkd_run_merge", "pkd_merge_states",
-                 "pkd_check_status", "pkd_run_static", "pkd_prefix_workspace_size",
-                 "pkd_plan_shared_prefix", "pkd_run_shared_prefix", "pkd_append_kv"):
+    lib.pkd_run_shared_prefix_states.argtypes = [ctypes.POINTER(PrefixPlan), vp, vp, vp,
+                                                 vp, vp, ctypes.c_size_t, ctypes.c_float,
+                                                 vp]
+    lib.pkd_run_cascade.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, vp, vp, vp,
+                                    ctypes.c_size_t, ctypes.POINTER(PrefixPlan), vp, vp,
+                                    ctypes.c_size_t, ctypes.c_float, vp, vp, vp]
+    lib.pkd_run_cascade_merge.argtypes = [ctypes.POINTER(Plan), vp, vp, ctypes.c_size_t,
+                                          ctypes.POINTER(PrefixPlan), vp, vp,
+                                          ctypes.c_size_t, vp, vp, vp]
+    for name in EXPORTED[2:]:
         getattr(lib, name).restype = ctypes.c_int
-    if lib.pkd_abi_version() != 2:
+    if lib.pkd_abi_version() != ABI_VERSION:
         raise RuntimeError("libpkd.so ABI version mismatch")
     _lib = lib
     return lib
@@ -370,6 +381,71 @@ def run_shared_prefix(plan_: PrefixPlan, q, k_pages, v_pages, int_ws, float_ws,
     return out, lse
 
 
+def run_shared_prefix_states(plan_: PrefixPlan, q, k_pages, v_pages, int_ws, float_ws,
+                             sm_scale: float, stream=None):
+    """The shared-prefix kernel alone: chunk states into ``float_ws``."""
+    p = plan_.problem
+    if _dtype_code(q.dtype) != p.dtype or k_pages.dtype != q.dtype or \
+            v_pages.dtype != q.dtype:
+        raise ValueError("dtype does not match the plan")
+    _check(load().pkd_run_shared_prefix_states(
+        ctypes.byref(plan_), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(int_ws),
+        _ptr(float_ws), float_ws.numel() * float_ws.element_size(), float(sm_scale),
+        _stream_ptr(stream)))
+
+
+def _state_buffers(p, q, out, lse):
+    import torch
+    if out is None:
+        out = torch.empty((p.batch, p.num_qo_heads, p.head_dim), dtype=q.dtype,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((p.batch, p.num_qo_heads), dtype=torch.float32,
+                          device=q.device)
+    if out.dtype != q.dtype or lse.dtype != torch.float32:
+        raise ValueError("out must have the query dtype and lse float32")
+    if not out.is_contiguous() or not lse.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return out, lse
+
+
+def run_cascade(plan_: Plan, prefix_plan: PrefixPlan, q, k_pages, v_pages, kv_indptr,
+                kv_indices, kv_last_page_len, ws, prefix_ws, sm_scale: float, out=None,
+                lse=None, stream=None):
+    """Attention over a shared prefix followed by each request's suffix.
+
+    ``plan_`` / ``ws`` (a :class:`Workspace`) are the suffix plan and its
+    buffers, ``kv_*`` the suffix pages; ``prefix_plan`` / ``prefix_ws`` (a
+    :class:`PrefixWorkspace`) the shared prefix.  Returns (out, lse).
+    """
+    out, lse = _state_buffers(plan_.problem, q, out, lse)
+    if _dtype_code(q.dtype) != plan_.problem.dtype or k_pages.dtype != q.dtype or \
+            v_pages.dtype != q.dtype:
+        raise ValueError("dtype does not match the plan")
+    fbytes = ws.float_ws.numel() * ws.float_ws.element_size()
+    pbytes = prefix_ws.float_ws.numel() * prefix_ws.float_ws.element_size()
+    _check(load().pkd_run_cascade(
+        ctypes.byref(plan_), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_indptr),
+        _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(ws.int_ws), _ptr(ws.float_ws),
+        fbytes, ctypes.byref(prefix_plan), _ptr(prefix_ws.int_ws),
+        _ptr(prefix_ws.float_ws), pbytes, float(sm_scale), _ptr(out), _ptr(lse),
+        _stream_ptr(stream)))
+    return out, lse
+
+
+def run_cascade_merge(plan_: Plan, prefix_plan: PrefixPlan, ws, prefix_ws, out, lse,
+                      stream=None):
+    """The last launch of :func:`run_cascade`: folds the prefix chunk states
+    into the suffix states in (out, lse)."""
+    fbytes = ws.float_ws.numel() * ws.float_ws.element_size()
+    pbytes = prefix_ws.float_ws.numel() * prefix_ws.float_ws.element_size()
+    _check(load().pkd_run_cascade_merge(
+        ctypes.byref(plan_), _ptr(ws.int_ws), _ptr(ws.float_ws), fbytes,
+        ctypes.byref(prefix_plan), _ptr(prefix_ws.int_ws), _ptr(prefix_ws.float_ws),
+        pbytes, _ptr(out), _ptr(lse), _stream_ptr(stream)))
+    return out, lse
+
+
 class PrefixWorkspace:
     """Workspaces and pinned staging for shared prefixes of a capacity."""
 
@@ -400,6 +476,10 @@ class PrefixWorkspace:
             stream=None):
         return run_shared_prefix(plan_, q, k_pages, v_pages, self.int_ws, self.float_ws,
                                  sm_scale, out=out, lse=lse, stream=stream)
+
+    def run_states(self, plan_: PrefixPlan, q, k_pages, v_pages, sm_scale, stream=None):
+        run_shared_prefix_states(plan_, q, k_pages, v_pages, self.int_ws, self.float_ws,
+                                 sm_scale, stream=stream)
 
 
 class Workspace:

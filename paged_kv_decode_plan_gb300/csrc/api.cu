@@ -60,6 +60,68 @@ pkd_status resolve_ctas(pkd_problem *p) {
   return PKD_OK;
 }
 
+// Checks a prefix plan's launch and starts the shared-prefix kernel, which
+// leaves each (request, head, chunk) state in the prefix float workspace.
+pkd_status start_prefix(const pkd_prefix_plan_t *plan, const void *q, const void *k_pages,
+                        const void *v_pages, void *int_ws_dev, void *float_ws_dev,
+                        size_t float_ws_bytes, float sm_scale, void *stream) {
+  if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "prefix plan not valid");
+  const pkd_problem &p = plan->problem;
+  pkd_status st = pkd::check_problem(p, true);
+  if (st != PKD_OK) return st;
+  if (p.batch == 0) return PKD_OK;
+  if (!q || !k_pages || !v_pages || !int_ws_dev || !float_ws_dev)
+    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
+    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
+  if (float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed))
+    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the prefix plan needs");
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f))
+    return fail(PKD_ERR_INVALID_ARG, "sm_scale must be finite and positive");
+  pkd::PrefixArgs a;
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.image = static_cast<int32_t *>(int_ws_dev);
+  a.partials = static_cast<float *>(float_ws_dev);
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.num_pages = p.num_pages;
+  a.batch = p.batch;
+  a.num_qo_heads = p.num_qo_heads;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  a.dtype = p.dtype;
+  a.length = plan->prefix_len;
+  a.chunks = plan->chunks;
+  a.chunk_tiles = plan->chunk_tiles;
+  a.row_tiles = plan->row_tiles;
+  a.layout = p.kv_layout;
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_shared_prefix(a, stream));
+  if (e == cudaErrorNotSupported)
+    return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");
+  if (e != cudaSuccess) return cuda_fail(e, "launching the shared-prefix kernel");
+  return PKD_OK;
+}
+
+// A suffix plan and a prefix plan that describe one cascade: the same
+// requests, heads and dtype over one page pool.
+pkd_status check_cascade(const pkd_plan_t *plan, const pkd_prefix_plan_t *prefix_plan) {
+  if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "plan not valid");
+  if (!prefix_plan || !prefix_plan->valid)
+    return fail(PKD_ERR_INVALID_ARG, "prefix plan not valid");
+  const pkd_problem &a = plan->problem, &b = prefix_plan->problem;
+  pkd_status st = pkd::check_problem(a, true);
+  if (st != PKD_OK) return st;
+  if (a.batch != b.batch || a.num_qo_heads != b.num_qo_heads ||
+      a.num_kv_heads != b.num_kv_heads || a.head_dim != b.head_dim || a.dtype != b.dtype ||
+      a.page_size != b.page_size || a.num_pages != b.num_pages ||
+      a.kv_layout != b.kv_layout)
+    return fail(PKD_ERR_INVALID_ARG,
+                "suffix and prefix plans differ in batch, heads, dtype or page pool");
+  return PKD_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -339,53 +401,107 @@ pkd_status pkd_plan_shared_prefix(const pkd_problem *problem,
   return PKD_OK;
 }
 
+pkd_status pkd_run_shared_prefix_states(const pkd_prefix_plan_t *plan, const void *q,
+                                        const void *k_pages, const void *v_pages,
+                                        void *int_ws_dev, void *float_ws_dev,
+                                        size_t float_ws_bytes, float sm_scale,
+                                        void *stream) {
+  pkd::clear_error();
+  return start_prefix(plan, q, k_pages, v_pages, int_ws_dev, float_ws_dev, float_ws_bytes,
+                      sm_scale, stream);
+}
+
 pkd_status pkd_run_shared_prefix(const pkd_prefix_plan_t *plan, const void *q,
                                  const void *k_pages, const void *v_pages,
                                  void *int_ws_dev, void *float_ws_dev,
                                  size_t float_ws_bytes, float sm_scale, void *out,
                                  float *lse, void *stream) {
   pkd::clear_error();
-  if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "plan not valid");
+  if (plan && plan->valid && plan->problem.batch > 0) {
+    if (!out || !lse) return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+    if (!aligned16(out)) return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
+  }
+  pkd_status st = start_prefix(plan, q, k_pages, v_pages, int_ws_dev, float_ws_dev,
+                               float_ws_bytes, sm_scale, stream);
+  if (st != PKD_OK || plan->problem.batch == 0) return st;
   const pkd_problem &p = plan->problem;
-  pkd_status st = pkd::check_problem(p, true);
-  if (st != PKD_OK) return st;
-  if (p.batch == 0) return PKD_OK;
-  if (!q || !k_pages || !v_pages || !int_ws_dev || !float_ws_dev || !out || !lse)
-    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
-  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
-      !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
-    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
-  if (float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed))
-    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the prefix plan needs");
-  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f))
-    return fail(PKD_ERR_INVALID_ARG, "sm_scale must be finite and positive");
-  pkd::PrefixArgs a;
-  a.q = q;
-  a.k_pages = k_pages;
-  a.v_pages = v_pages;
-  a.image = static_cast<int32_t *>(int_ws_dev);
-  a.partials = static_cast<float *>(float_ws_dev);
-  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-  a.num_pages = p.num_pages;
-  a.batch = p.batch;
-  a.num_qo_heads = p.num_qo_heads;
-  a.num_kv_heads = p.num_kv_heads;
-  a.page_size = p.page_size;
-  a.dtype = p.dtype;
-  a.length = plan->prefix_len;
-  a.chunks = plan->chunks;
-  a.chunk_tiles = plan->chunk_tiles;
-  a.row_tiles = plan->row_tiles;
-  a.layout = p.kv_layout;
-  cudaError_t e = static_cast<cudaError_t>(pkd::launch_shared_prefix(a, stream));
-  if (e == cudaErrorNotSupported)
-    return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");
-  if (e != cudaSuccess) return cuda_fail(e, "launching the shared-prefix kernel");
-  e = static_cast<cudaError_t>(pkd::launch_merge_uniform(
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_merge_uniform(
       static_cast<const float *>(float_ws_dev), out, lse, p.batch, p.num_qo_heads,
       plan->chunks, p.dtype, 4 * p.num_ctas, stream));
   if (e != cudaSuccess) return cuda_fail(e, "launching the prefix merge");
   return PKD_OK;
+}
+
+pkd_status pkd_run_cascade_merge(const pkd_plan_t *plan, void *int_ws_dev,
+                                 const void *float_ws_dev, size_t float_ws_bytes,
+                                 const pkd_prefix_plan_t *prefix_plan,
+                                 const void *prefix_int_ws_dev,
+                                 const void *prefix_float_ws_dev,
+                                 size_t prefix_float_ws_bytes, void *out, float *lse,
+                                 void *stream) {
+  pkd::clear_error();
+  pkd_status st = check_cascade(plan, prefix_plan);
+  if (st != PKD_OK) return st;
+  const pkd_problem &p = plan->problem;
+  if (p.batch == 0) return PKD_OK;
+  if (!int_ws_dev || !prefix_int_ws_dev || !prefix_float_ws_dev || !out || !lse)
+    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned16(out) || !aligned16(int_ws_dev) || !aligned16(float_ws_dev) ||
+      !aligned16(prefix_int_ws_dev) || !aligned16(prefix_float_ws_dev))
+    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
+  if (prefix_float_ws_bytes < static_cast<size_t>(prefix_plan->float_ws_bytes_needed))
+    return fail(PKD_ERR_WORKSPACE, "prefix float workspace smaller than its plan needs");
+  const bool capture = capturing(stream);
+  if ((plan->num_partials > 0 || capture) &&
+      (!float_ws_dev || float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed)))
+    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the plan needs");
+  const Bounds bounds = launch_bounds(*plan, float_ws_bytes, capture);
+  pkd::CascadeMergeArgs m;
+  m.image = static_cast<const int32_t *>(int_ws_dev);
+  m.partials = static_cast<const float *>(float_ws_dev);
+  m.prefix_image = static_cast<const int32_t *>(prefix_int_ws_dev);
+  m.prefix_partials = static_cast<const float *>(prefix_float_ws_dev);
+  m.out = out;
+  m.lse = lse;
+  m.num_qo_heads = p.num_qo_heads;
+  m.dtype = p.dtype;
+  m.grid = 4 * p.num_ctas;  // upper bound on CTAs; rows loop inside
+  m.batch = p.batch;
+  m.chunks = prefix_plan->chunks;
+  m.max_partials = bounds.max_partials;
+  m.image_words = bounds.image_words;
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_cascade_merge(m, stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the cascade merge");
+  return PKD_OK;
+}
+
+pkd_status pkd_run_cascade(const pkd_plan_t *plan, const void *q, const void *k_pages,
+                           const void *v_pages, const int32_t *kv_indptr_d,
+                           const int32_t *kv_indices_d,
+                           const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                           void *float_ws_dev, size_t float_ws_bytes,
+                           const pkd_prefix_plan_t *prefix_plan, void *prefix_int_ws_dev,
+                           void *prefix_float_ws_dev, size_t prefix_float_ws_bytes,
+                           float sm_scale, void *out, float *lse, void *stream) {
+  pkd::clear_error();
+  // every host-side check before the first launch
+  pkd_status st = check_cascade(plan, prefix_plan);
+  if (st != PKD_OK) return st;
+  if (plan->problem.batch == 0) return PKD_OK;
+  if (!out || !lse || !prefix_float_ws_dev)
+    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (prefix_float_ws_bytes < static_cast<size_t>(prefix_plan->float_ws_bytes_needed))
+    return fail(PKD_ERR_WORKSPACE, "prefix float workspace smaller than its plan needs");
+  st = start_prefix(prefix_plan, q, k_pages, v_pages, prefix_int_ws_dev,
+                    prefix_float_ws_dev, prefix_float_ws_bytes, sm_scale, stream);
+  if (st != PKD_OK) return st;
+  st = pkd_run_decode(plan, q, k_pages, v_pages, kv_indptr_d, kv_indices_d,
+                      kv_last_page_len_d, int_ws_dev, float_ws_dev, float_ws_bytes,
+                      sm_scale, out, lse, stream);
+  if (st != PKD_OK) return st;
+  return pkd_run_cascade_merge(plan, int_ws_dev, float_ws_dev, float_ws_bytes, prefix_plan,
+                               prefix_int_ws_dev, prefix_float_ws_dev,
+                               prefix_float_ws_bytes, out, lse, stream);
 }
 
 pkd_status pkd_check_status(const void *int_ws_dev, uint32_t *device_status,

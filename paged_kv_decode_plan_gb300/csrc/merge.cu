@@ -10,6 +10,7 @@
 // correction": no -inf - (-inf) reaches exp).
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 
 #include "pkd_internal.h"
@@ -21,9 +22,29 @@ namespace {
 constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = 32 * kMergeWarps;
 
+// Folds one state (lse s, normalised output v) into a running (m, ws, acc)
+// by the online rule: a new maximum rescales what was folded so far; a state
+// with s = -inf has weight 0.
+__device__ __forceinline__ void fold_one(float s, float4 v, float &m, float &ws, float4 &acc) {
+  if (s > m) {
+    const float f = m == -INFINITY ? 0.f : expf(m - s);
+    acc.x *= f;
+    acc.y *= f;
+    acc.z *= f;
+    acc.w *= f;
+    ws *= f;
+    m = s;
+  }
+  const float w = s == -INFINITY ? 0.f : expf(s - m);
+  acc.x += w * v.x;
+  acc.y += w * v.y;
+  acc.z += w * v.z;
+  acc.w += w * v.w;
+  ws += w;
+}
+
 // Folds partial states s0, s0 + stride, ... (< s1) of query head h into a
-// running (m, ws, acc) by the online rule: a new maximum rescales what was
-// folded so far; kUnroll states' loads are in flight per step.
+// running (m, ws, acc); kUnroll states' loads are in flight per step.
 template <int kUnroll = 4>
 __device__ __forceinline__ void fold_states(const float *partials, long long slot_floats,
                                             int hq, int h, int s0, int s1, int stride,
@@ -43,23 +64,7 @@ __device__ __forceinline__ void fold_states(const float *partials, long long slo
       }
     }
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-      if (sv[k] > m) {
-        const float f = m == -INFINITY ? 0.f : expf(m - sv[k]);
-        acc.x *= f;
-        acc.y *= f;
-        acc.z *= f;
-        acc.w *= f;
-        ws *= f;
-        m = sv[k];
-      }
-      const float w = sv[k] == -INFINITY ? 0.f : expf(sv[k] - m);
-      acc.x += w * ov[k].x;
-      acc.y += w * ov[k].y;
-      acc.z += w * ov[k].z;
-      acc.w += w * ov[k].w;
-      ws += w;
-    }
+    for (int k = 0; k < kUnroll; ++k) fold_one(sv[k], ov[k], m, ws, acc);
   }
 }
 
@@ -96,6 +101,77 @@ __global__ void __launch_bounds__(kMergeThreads)
     // a request's chunks are read in one round (the partials sit in L2)
     fold_states<8>(partials, slot_floats, hq, h, b * chunks, (b + 1) * chunks, 1, lane, m,
                    ws, acc);
+    write_state<T>(out, lse, b, hq, h, lane, m, ws, acc);
+  }
+}
+
+// Cascade merge ("FlashInfer" (aiwiki.ai/wiki/flashinfer), "Attention
+// states": the states of the shared prefix and of a request's own suffix
+// merge into the state over both).  One warp per (request b, query head h)
+// row folds the prefix's chunk states (slots b * chunks .. b * chunks +
+// chunks - 1 of the prefix workspace) and the suffix state: the request's
+// partial slots if the suffix plan split it, else the (out, lse) row the
+// decode kernel wrote, which is read before the final state overwrites it.
+// The suffix plan lists its split requests in increasing order; a warp finds
+// b among them 32 at a time with a ballot.
+template <typename T>
+__global__ void __launch_bounds__(kMergeThreads)
+    cascade_merge_kernel(const int32_t *image, const float *partials,
+                         const int32_t *prefix_image, const float *prefix_partials,
+                         uint16_t *out, float *lse, int hq, int batch, int chunks,
+                         int max_partials, int image_words) {
+  const int lane = threadIdx.x & 31;
+  const int num_ctas = image[kHNumCtas];
+  const int num_units = image[kHNumUnits];
+  const int num_split = image[kHNumSplit];
+  const int num_partials = image[kHNumPartials];
+  const ImageOffsets o = image_offsets(num_ctas, num_units, num_split);
+  // both images must be the plans the host made for this launch
+  if (image[kHMagic] != kMagic || image[kHBatch] != batch || image[kHNumQoHeads] != hq ||
+      num_ctas < 0 || num_units < 0 || num_split < 0 || num_partials < 0 ||
+      num_partials > max_partials || o.end > image_words ||
+      prefix_image[kHMagic] != kPrefixMagic || prefix_image[kPBatch] != batch ||
+      prefix_image[kPNumQoHeads] != hq || prefix_image[kPChunks] != chunks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      atomicOr(reinterpret_cast<unsigned int *>(const_cast<int32_t *>(image) + kHStatus),
+               PKD_DEVICE_BAD_PLAN);
+    return;
+  }
+  const int32_t *merge_indptr = image + o.merge_indptr;
+  const int32_t *merge_req = image + o.merge_req;
+  const long long slot_floats = partial_slot_floats(hq, kHeadDim);
+  const long long rows = static_cast<long long>(batch) * hq;
+  // a programmatic dependent of the decode kernel, which started after the
+  // prefix kernel had finished: once the decode kernel is complete, both
+  // kernels' states are in place
+  ptx::wait_primary_grid();
+  for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       row < rows; row += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+    const int b = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
+    int split = -1;
+    for (int base = 0; base < num_split; base += 32) {
+      const int r = base + lane < num_split ? merge_req[base + lane] : INT_MAX;
+      const unsigned hit = __ballot_sync(0xffffffffu, r == b);
+      if (hit) {
+        split = base + __ffs(hit) - 1;
+        break;
+      }
+      if (__shfl_sync(0xffffffffu, r, 31) > b) break;  // past b: not split
+    }
+    float m = -INFINITY, ws = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    fold_states<8>(prefix_partials, slot_floats, hq, h, b * chunks, (b + 1) * chunks, 1,
+                   lane, m, ws, acc);
+    if (split >= 0) {
+      const int s0 = max(0, merge_indptr[split]);
+      const int s1 = min(num_partials, merge_indptr[split + 1]);
+      fold_states(partials, slot_floats, hq, h, s0, s1, 1, lane, m, ws, acc);
+    } else {
+      const uint2 raw = reinterpret_cast<const uint2 *>(out + row * kHeadDim)[lane];
+      const float2 v01 = ptx::unpack2<T>(raw.x), v23 = ptx::unpack2<T>(raw.y);
+      fold_one(lse[row], make_float4(v01.x, v01.y, v23.x, v23.y), m, ws, acc);
+    }
+    __syncwarp();  // every lane has read the row before it is overwritten
     write_state<T>(out, lse, b, hq, h, lane, m, ws, acc);
   }
 }
@@ -331,6 +407,32 @@ int launch_merge_uniform(const float *partials, void *out, float *lse, int batch
                                            partials, o, lse, batch, hq, chunks)
                       : cudaLaunchKernelEx(&cfg, merge_uniform_kernel<__half>, partials,
                                            o, lse, batch, hq, chunks);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+int launch_cascade_merge(const CascadeMergeArgs &a, void *stream) {
+  const long long rows = static_cast<long long>(a.batch) * a.num_qo_heads;
+  if (rows == 0) return cudaSuccess;
+  const long long want = (rows + kMergeWarps - 1) / kMergeWarps;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < a.grid ? want : a.grid));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  uint16_t *o = static_cast<uint16_t *>(a.out);
+  cudaError_t e =
+      a.dtype == PKD_BF16
+          ? cudaLaunchKernelEx(&cfg, cascade_merge_kernel<__nv_bfloat16>, a.image, a.partials,
+                               a.prefix_image, a.prefix_partials, o, a.lse, a.num_qo_heads,
+                               a.batch, a.chunks, a.max_partials, a.image_words)
+          : cudaLaunchKernelEx(&cfg, cascade_merge_kernel<__half>, a.image, a.partials,
+                               a.prefix_image, a.prefix_partials, o, a.lse, a.num_qo_heads,
+                               a.batch, a.chunks, a.max_partials, a.image_words);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

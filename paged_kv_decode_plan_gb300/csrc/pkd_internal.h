@@ -140,6 +140,19 @@ struct PrefixArgs {
 int launch_shared_prefix(const PrefixArgs &a, void *stream);
 int launch_merge_uniform(const float *partials, void *out, float *lse, int batch, int hq,
                          int chunks, int dtype, int grid, void *stream);
+// Cascade merge (merge.cu): prefix chunk states + suffix states -> out, lse.
+struct CascadeMergeArgs {
+  const int32_t *image;          // suffix plan image
+  const float *partials;         // suffix partial states
+  const int32_t *prefix_image;   // prefix plan image
+  const float *prefix_partials;  // prefix chunk states
+  void *out;
+  float *lse;
+  int num_qo_heads, dtype, grid;
+  int batch, chunks;             // of the prefix plan (the suffix image must agree)
+  int max_partials, image_words; // bounds for the suffix image
+};
+int launch_cascade_merge(const CascadeMergeArgs &a, void *stream);
 pkd_status plan_prefix_impl(const pkd_problem &in, const int32_t *pages,
                             int32_t num_prefix_pages, int32_t last_page_len,
                             pkd_prefix_plan_t *plan, int32_t *image, size_t image_bytes);
