@@ -209,15 +209,10 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int32_t *merge_req = image + o.merge_req;
   const long long slot_floats = partial_slot_floats(hq, kHeadDim);
   const long long rows = static_cast<long long>(num_split) * hq;
-  // launched as a programmatic dependent of the decode kernel: the plan image
-  // was in place before that kernel started, the partial states are only
-  // complete once it has finished
-  ptx::wait_primary_grid();
-
-  for (long long first = static_cast<long long>(blockIdx.x) * kRowsPerCta; first < rows;
-       first += static_cast<long long>(gridDim.x) * kRowsPerCta) {
-    const long long row = first + slot_in_cta;
-    int b = -1, h = 0, s0 = 0, s1 = 0;
+  // (request, head, slot range) of a row, from the plan image alone
+  auto describe = [&](long long row, int &b, int &h, int &s0, int &s1) {
+    b = -1;
+    h = s0 = s1 = 0;
     if (row < rows) {
       const int i = static_cast<int>(row / hq);
       h = static_cast<int>(row % hq);
@@ -226,6 +221,19 @@ __global__ void __launch_bounds__(kMergeThreads)
       s1 = min(num_partials, merge_indptr[i + 1]);
       if (b < 0 || b >= image[kHBatch]) b = -1;
     }
+  };
+  // launched as a programmatic dependent of the decode kernel: the plan image
+  // was in place before that kernel started, so the first row's description
+  // is read before the wait; the partial states are only complete once the
+  // decode kernel has finished
+  long long first = static_cast<long long>(blockIdx.x) * kRowsPerCta;
+  int b, h, s0, s1;
+  describe(first + slot_in_cta, b, h, s0, s1);
+  ptx::wait_primary_grid();
+
+  for (; first < rows; first += static_cast<long long>(gridDim.x) * kRowsPerCta) {
+    if (first != static_cast<long long>(blockIdx.x) * kRowsPerCta)
+      describe(first + slot_in_cta, b, h, s0, s1);
     float m = -INFINITY, ws = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (b >= 0)
