@@ -56,6 +56,11 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kStageBudget = 200 * 1024;            // bytes of stages per CTA
+// With pages of fewer than 16 tokens every tile needs fresh page ids (16 at
+// P = 1, a new half line of the page table): the bulk loader prefetches the
+// page-id line this many tiles ahead into L2, so the id load of a tile, on
+// which its copies wait, hits L2 instead of HBM.
+constexpr int kIdPrefetchTiles = 4;
 
 enum Loader : int { kLoaderTma = PKD_LOADER_TMA_TILES, kLoaderBulk = PKD_LOADER_BULK_ROWS };
 
@@ -247,6 +252,10 @@ __device__ void load_bulk(const Params &p, const int32_t *units, int num_partial
       slot = tok - pi * p.page_size;
       page = __ldg(p.indices + unit.pbase + pi);
     }
+    // within this unit only: its page ids are inside the request's range
+    const int ahead = tok + kIdPrefetchTiles * kTile;
+    if (p.page_size < kTile && ahead < t1)
+      ptx::prefetch_l2(p.indices + unit.pbase + ahead / p.page_size);
     ++t;
   };
   describe();
