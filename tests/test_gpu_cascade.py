@@ -42,11 +42,11 @@ def _reference(wl, prefix, suffix):
     return oracle.merge(po, ps, so, ss)
 
 
-def _setup(wl, pre_pages, pre_last, suffix, num_ctas, min_chunks):
+def _setup(wl, pre_pages, pre_last, suffix, num_ctas, min_chunks, layout=pkd.LAYOUT_NHD):
     prob = pkd.make_problem(batch=wl.batch, num_qo_heads=wl.num_qo_heads,
                             num_kv_heads=wl.num_kv_heads, page_size=wl.page_size,
                             dtype=wl.dtype, num_pages=wl.num_pages, num_ctas=num_ctas,
-                            min_chunks_per_request=min_chunks)
+                            min_chunks_per_request=min_chunks, kv_layout=layout)
     ws = pkd.Workspace(prob)
     plan = ws.plan(suffix.kv_indptr, suffix.kv_last_page_len, suffix.kv_indices)
     pws = pkd.PrefixWorkspace(prob, max(1, pre_pages.size))
@@ -185,3 +185,26 @@ def test_captured_cascade_follows_later_suffix_plans():
         torch.cuda.synchronize()
         assert pkd.check_status(ws.int_ws) == 0 and pkd.check_status(pws.int_ws) == 0
         gh.compare(out, lse, *_reference(wl, prefix, t), "f16")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_cascade_hnd_pages_equal_nhd(dtype):
+    # the same values in [pages][Hkv][P][D]: the same bits as the NHD run
+    wl, pre_pages, pre_last, prefix, suffix = _case(4, 32, 8, 16, 600, [30, 900, 0, 2500],
+                                                    dtype, 13)
+    dev = gh.DeviceBatch(wl)
+    indptr, indices, last = gh.device_table(suffix)
+    results = []
+    for layout in (pkd.LAYOUT_NHD, pkd.LAYOUT_HND):
+        k, v = dev.k, dev.v
+        if layout == pkd.LAYOUT_HND:
+            k, v = k.transpose(1, 2).contiguous(), v.transpose(1, 2).contiguous()
+        ws, plan, pws, pplan = _setup(wl, pre_pages, pre_last, suffix, 12, 1, layout)
+        out, lse = pkd.run_cascade(plan, pplan, dev.q, k, v, indptr, indices, last, ws, pws,
+                                   wl.sm_scale)
+        torch.cuda.synchronize()
+        assert pkd.check_status(ws.int_ws) == 0 and pkd.check_status(pws.int_ws) == 0
+        results.append((out, lse))
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.equal(results[0][1], results[1][1])
+    gh.compare(results[1][0], results[1][1], *_reference(wl, prefix, suffix), dtype)
