@@ -1,0 +1,109 @@
+"""Host-side argument checks of the cascade entry points (no GPU needed).
+
+pkd_run_cascade, pkd_run_cascade_merge and pkd_run_shared_prefix_states
+check plans, problem agreement, pointers and workspace sizes on the host and
+return a status before any CUDA call; these tests pass placeholder device
+addresses that a launch would need, so a check that let them through would
+fail here loudly rather than touch memory.
+"""
+import ctypes
+
+import numpy as np
+
+import paged_kv_decode_plan_gb300 as pkd
+
+INVALID_ARG, WORKSPACE = -1, -3
+FAKE = ctypes.c_void_p(0x10000)  # 16-byte aligned placeholder, never dereferenced
+
+
+def _suffix_plan(batch=3, dtype="f16"):
+    prob = pkd.make_problem(batch=batch, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                            dtype=dtype, num_pages=64, num_ctas=8)
+    lengths = [40, 300, 17][:batch]
+    npages = [(n + 15) // 16 for n in lengths]
+    indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
+    last = np.array([n - (p - 1) * 16 for n, p in zip(lengths, npages)], dtype=np.int32)
+    plan, _ = pkd.plan_host(prob, indptr, last)
+    return plan
+
+
+def _prefix_plan(suffix, **override):
+    """A prefix plan as pkd_plan_shared_prefix would describe a one-page prefix."""
+    pp = pkd.PrefixPlan()
+    pp.problem = pkd.Problem.from_buffer_copy(suffix.problem)
+    for k, v in override.items():
+        setattr(pp.problem, k, v)
+    pp.prefix_len, pp.prefix_num_pages, pp.chunks, pp.chunk_tiles = 16, 1, 1, 1
+    pp.row_tiles = 1
+    pp.num_blocks = pp.problem.num_kv_heads
+    pp.int_ws_bytes_used = 4 * 17
+    pp.float_ws_bytes_needed = 4 * pp.problem.batch * (32 * 128 + 32)
+    pp.valid = 1
+    return pp
+
+
+def _cascade(plan, pp, out=FAKE, lse=FAKE, prefix_float=FAKE, prefix_bytes=1 << 30):
+    lib = pkd.load()
+    return lib.pkd_run_cascade(ctypes.byref(plan), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               FAKE, 1 << 30, ctypes.byref(pp), FAKE, prefix_float,
+                               prefix_bytes, ctypes.c_float(0.088), out, lse, None)
+
+
+def _message():
+    return pkd.load().pkd_last_error().decode()
+
+
+def test_cascade_rejects_an_invalid_prefix_plan():
+    plan = _suffix_plan()
+    pp = _prefix_plan(plan)
+    pp.valid = 0
+    assert _cascade(plan, pp) == INVALID_ARG
+    assert "prefix plan" in _message()
+
+
+def test_cascade_rejects_plans_that_disagree():
+    plan = _suffix_plan()
+    for field, value in [("batch", 2), ("num_qo_heads", 64), ("dtype", pkd.PKD_BF16),
+                         ("page_size", 32), ("num_pages", 65),
+                         ("kv_layout", pkd.LAYOUT_HND)]:
+        pp = _prefix_plan(plan, **{field: value})
+        assert _cascade(plan, pp) == INVALID_ARG, field
+        assert "differ" in _message(), field
+
+
+def test_cascade_checks_pointers_and_prefix_workspace():
+    plan = _suffix_plan()
+    pp = _prefix_plan(plan)
+    assert _cascade(plan, pp, out=None) == INVALID_ARG
+    assert _cascade(plan, pp, prefix_float=None) == INVALID_ARG
+    assert _cascade(plan, pp, prefix_bytes=pp.float_ws_bytes_needed - 1) == WORKSPACE
+    assert "prefix float workspace" in _message()
+
+
+def test_cascade_merge_checks_before_launching():
+    plan = _suffix_plan()
+    lib = pkd.load()
+    pp = _prefix_plan(plan, batch=1)
+    assert lib.pkd_run_cascade_merge(ctypes.byref(plan), FAKE, FAKE, 1 << 30,
+                                     ctypes.byref(pp), FAKE, FAKE, 1 << 30, FAKE, FAKE,
+                                     None) == INVALID_ARG
+    pp = _prefix_plan(plan)
+    assert lib.pkd_run_cascade_merge(ctypes.byref(plan), FAKE, FAKE, 1 << 30,
+                                     ctypes.byref(pp), FAKE, FAKE, 8, FAKE, FAKE,
+                                     None) == WORKSPACE
+
+
+def test_prefix_states_check_the_plan_and_pointers():
+    plan = _suffix_plan()
+    lib = pkd.load()
+    pp = _prefix_plan(plan)
+    pp.valid = 0
+    assert lib.pkd_run_shared_prefix_states(ctypes.byref(pp), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                            1 << 30, ctypes.c_float(0.088),
+                                            None) == INVALID_ARG
+    pp = _prefix_plan(plan)
+    assert lib.pkd_run_shared_prefix_states(ctypes.byref(pp), None, FAKE, FAKE, FAKE, FAKE,
+                                            1 << 30, ctypes.c_float(0.088),
+                                            None) == INVALID_ARG
+    assert lib.pkd_run_shared_prefix_states(ctypes.byref(pp), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                            8, ctypes.c_float(0.088), None) == WORKSPACE
