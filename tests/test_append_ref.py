@@ -62,3 +62,33 @@ def test_append_order_does_not_matter_and_out_of_range_is_skipped():
     _, _, skipped = append_ref.append_kv(k, v, kn[:4], vn[:4], bad_bi, bad_pos,
                                          indptr, indices, last)
     assert skipped == [0, 2, 3]
+
+
+def test_appended_token_is_what_its_request_attends_to():
+    # Pinned through the attention oracle's own page-table walk (ref_attn.c,
+    # pinned against brute force): a new key that outscores every other key
+    # of its request by > 100 makes attention over the request return the new
+    # value; requests that received nothing are not pulled toward it.
+    import math
+    import oracle
+    rng = np.random.default_rng(2)
+    lengths = [5, 17, 1, 33, 9]
+    page, hkv, g, d = 4, 2, 2, 8
+    k, v, indptr, indices, last = _case(rng, lengths, page, hkv, d)
+    q = np.repeat(rng.standard_normal((len(lengths), hkv, 1, d)), g, axis=2)
+    q = q.reshape(len(lengths), hkv * g, d)           # the group's query heads agree
+    bi = np.array([0, 1, 2, 3], np.int32)
+    pos = np.array([4, 16, 0, 32], np.int32)           # each request's last slot
+    kn = 40.0 * q[bi][:, ::g, :]                        # [new token, Hkv, D]
+    vn = rng.standard_normal((bi.size, hkv, d))
+    k2, v2, skipped = append_ref.append_kv(k.astype(np.float64), v.astype(np.float64), kn, vn,
+                                           bi, pos, indptr, indices, last)
+    assert skipped == []
+    out, _ = oracle.decode(q, k2, v2, indptr, indices, last, dtype="f64",
+                           sm_scale=1.0 / math.sqrt(d))
+    out = out.reshape(len(lengths), hkv * g, d)
+    for i, b in enumerate(bi):
+        for h in range(hkv * g):
+            assert np.max(np.abs(out[b, h] - vn[i, h // g])) <= 1e-12
+    for h in range(hkv * g):   # request 4 got no token
+        assert min(np.max(np.abs(out[4, h] - vn[i, h // g])) for i in range(bi.size)) > 0.1
