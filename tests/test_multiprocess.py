@@ -36,7 +36,7 @@ def _worker(rank, world, port, results):
 def test_two_gloo_ranks_aggregate_bytes_over_slowest_time():
     world = 2
     port = _free_port()
-    with mp.Manager() as manager:
+    with mp.get_context("spawn").Manager() as manager:
         results = manager.dict()
         mp.start_processes(_worker, args=(world, port, results), nprocs=world,
                            join=True, start_method="spawn")
