@@ -389,6 +389,14 @@ __device__ void load_q(const PrefixParams &p, int q, int h, int rt, uint8_t *sme
   ptx::mbar_arrive(bars.q_full(q));
 }
 
+// 256-bit global store (sm_100 and later); p must be 32-byte aligned.
+__device__ __forceinline__ void store8(float *p, float a, float b, float c, float d, float e,
+                                       float f, float g, float h) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(p), "f"(a),
+               "f"(b), "f"(c), "f"(d), "f"(e), "f"(f), "f"(g), "f"(h)
+               : "memory");
+}
+
 // Warps 4q .. 4q + 3: query tile q, softmax, and the chunk's partial states.
 template <typename T>
 __device__ void softmax_rows(const PrefixParams &p, int q, int h, int rt, int c, int t_begin,
@@ -456,14 +464,25 @@ __device__ void softmax_rows(const PrefixParams &p, int q, int h, int rt, int c,
   }
   tc::fence_after_sync();
   const float inv = l > 0.f ? 1.f / l : 0.f;
+  // Each thread writes its own row: whole 32-byte sectors (256-bit stores)
+  // where the row is 32-byte aligned, which halves the sector writes of
+  // 16-byte stores and leaves none half-filled.
+  const bool wide = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
 #pragma unroll 1
-  for (int cc = 0; cc < kHeadDim / 16; ++cc) {
-    float v[16];
-    tc::ld16(t_o + 16 * cc, v);
-    if (live) {
+  for (int half = 0; half < 2; ++half) {
+    float v[64];
+    tc::ld64(t_o + 64 * half, v);
+    if (!live) continue;
+    float *dst = o + 64 * half;
+    if (wide) {
 #pragma unroll
-      for (int e = 0; e < 16; e += 4)
-        *reinterpret_cast<float4 *>(o + 16 * cc + e) =
+      for (int e = 0; e < 64; e += 8)
+        store8(dst + e, v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv,
+               v[e + 4] * inv, v[e + 5] * inv, v[e + 6] * inv, v[e + 7] * inv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; e += 4)
+        *reinterpret_cast<float4 *>(dst + e) =
             make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
     }
   }
