@@ -615,7 +615,11 @@ def run_ours(args, ranks):
                      "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(wl.name),
+                     # the committed captures ran the default launch (NHD pages,
+                     # auto loader, full workload)
+                     "traffic": (profiled_traffic(wl.name)
+                                 if args.layout == "nhd" and args.loader == "auto"
+                                 and args.batch is None else None),
                      "algorithmic_bytes_per_launch": runner.decode_kv_bytes()},
         "e2e": e2e,
         "gpu_launches": runner.launches_per_step * k,

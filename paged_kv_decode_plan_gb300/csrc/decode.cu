@@ -215,8 +215,10 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
 
 // One 1-D bulk copy per (tensor, token) row: lane l moves row l & 15 of K
 // (l < 16) or V (l >= 16); for HND pages one copy per (tensor, token, head).
-// Page ids are loaded one tile ahead.
-template <int HKV>
+// Page ids are loaded one tile ahead; kSmallPages (pages of fewer than 16
+// tokens) adds the page-id prefetch, a separate instantiation so that the
+// loop for larger pages carries none of its instructions.
+template <int HKV, bool kSmallPages>
 __device__ void load_bulk(const Params &p, const int32_t *units, int num_partials,
                           int u_begin, int u_end, uint8_t *stages, uint32_t full0,
                           uint32_t empty0, volatile int *abort) {
@@ -252,10 +254,11 @@ __device__ void load_bulk(const Params &p, const int32_t *units, int num_partial
       slot = tok - pi * p.page_size;
       page = __ldg(p.indices + unit.pbase + pi);
     }
-    // within this unit only: its page ids are inside the request's range
-    const int ahead = tok + kIdPrefetchTiles * kTile;
-    if (p.page_size < kTile && ahead < t1)
-      ptx::prefetch_l2(p.indices + unit.pbase + ahead / p.page_size);
+    if constexpr (kSmallPages) {
+      // within this unit only: its page ids are inside the request's range
+      const int ahead = tok + kIdPrefetchTiles * kTile;
+      if (ahead < t1) ptx::prefetch_l2(p.indices + unit.pbase + ahead / p.page_size);
+    }
     ++t;
   };
   describe();
@@ -594,9 +597,12 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
     if (LOADER == kLoaderTma)
       load_tma<HKV>(q, &map_k, &map_v, units, num_partials, u_begin, u_end, stages,
                     full0, empty0, abort);
+    else if (q.page_size < kTile)
+      load_bulk<HKV, true>(q, units, num_partials, u_begin, u_end, stages, full0, empty0,
+                           abort);
     else
-      load_bulk<HKV>(q, units, num_partials, u_begin, u_end, stages, full0, empty0,
-                     abort);
+      load_bulk<HKV, false>(q, units, num_partials, u_begin, u_end, stages, full0, empty0,
+                            abort);
   } else {
     consume<T, HKV, NG, LOADER>(q, units, num_partials, u_begin, u_end, stages, full0,
                                 empty0, abort);
@@ -709,8 +715,8 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
     const void *k, *v;
     long long num_pages;
     int page_size, hkv, layout;
-    alignas(64) CUtensorMap mk;
-    alignas(64) CUtensorMap mv;
+    CUtensorMap mk;
+    CUtensorMap mv;
   };
   static std::mutex mutex;
   static Entry cache[8];
@@ -785,8 +791,8 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   prm.grid = a.num_ctas;
   prm.hnd = a.layout == PKD_LAYOUT_HND;
 
-  alignas(64) CUtensorMap mk;
-  alignas(64) CUtensorMap mv;
+  CUtensorMap mk;
+  CUtensorMap mv;
   std::memset(&mk, 0, sizeof(mk));
   std::memset(&mv, 0, sizeof(mv));
   // NHD: bulk rows unless TMA tiles were asked for.  HND: TMA tiles when

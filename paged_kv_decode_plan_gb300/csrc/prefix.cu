@@ -608,8 +608,8 @@ cudaError_t launch_typed(const PrefixParams &p, const CUtensorMap &mk, const CUt
 }  // namespace
 
 int launch_shared_prefix(const PrefixArgs &a, void *stream) {
-  alignas(64) CUtensorMap mk;
-  alignas(64) CUtensorMap mv;
+  CUtensorMap mk;
+  CUtensorMap mv;
   if (!page_tensor_maps(&mk, &mv, a.k_pages, a.v_pages, a.num_pages, a.page_size,
                         a.num_kv_heads, a.layout))
     return cudaErrorNotSupported;
@@ -632,7 +632,7 @@ int launch_shared_prefix(const PrefixArgs &a, void *stream) {
   p.chunk_tiles = a.chunk_tiles;
   p.row_tiles = a.row_tiles;
   p.hnd = a.layout == PKD_LAYOUT_HND;
-  alignas(64) CUtensorMap mq;
+  CUtensorMap mq;
   p.q_tma = query_tensor_map(&mq, a.q, a.batch, a.num_qo_heads, p.group) ? 1 : 0;
   if (!p.q_tma) std::memset(&mq, 0, sizeof(mq));
   const int grid = a.num_kv_heads * a.row_tiles * a.chunks;
