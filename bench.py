@@ -7,7 +7,12 @@ decode kernel, and the split-KV merge kernel (by default replayed as one CUDA
 graph per workspace; ``--graph off`` launches them one by one).  The default workload is the
 64-request batch (lengths uniform on [128, 4096], Hq 32 / Hkv 8, head_dim 128,
 page_size 16, fp16); ``--workload`` selects another of
-paged_kv_decode_plan_gb300.workloads.
+paged_kv_decode_plan_gb300.workloads.  For the cascade workload a step plans
+the suffix table and the shared prefix and runs the shared-prefix kernel, the
+suffix decode and the cascade merge (``--cascade fused``, pkd_run_cascade's
+launches), or the prefix and suffix runs merged by merge_states
+(``--cascade shared``), or the prefix listed in every request's table
+(``--cascade per-request``).
 
 Rank 0 prints one JSON line.  Under torchrun every rank runs the same batch
 on its own GPU (weak scaling, no data-path collective); timing is the maximum
