@@ -112,11 +112,12 @@ struct Unit {
 __device__ Unit read_unit(const Params &p, const int32_t *units, int u,
                           int num_partials) {
   const int32_t *w = units + kUnitWords * u;
+  const uint64_t keep = ptx::policy_evict_last();
   Unit r;
-  r.req = __ldg(w);
-  r.t0 = __ldg(w + 1);
-  r.t1 = __ldg(w + 2);
-  r.slot = __ldg(w + 3);
+  r.req = ptx::ldg_keep(w, keep);
+  r.t0 = ptx::ldg_keep(w + 1, keep);
+  r.t1 = ptx::ldg_keep(w + 2, keep);
+  r.slot = ptx::ldg_keep(w + 3, keep);
   r.pbase = 0;
   if (r.req < 0 || r.req >= p.batch || r.slot < -1 || r.slot >= num_partials ||
       r.t0 < 0 || r.t1 < r.t0) {
@@ -125,11 +126,11 @@ __device__ Unit read_unit(const Params &p, const int32_t *units, int u,
     r.t0 = r.t1 = 0;
     return r;
   }
-  const int pb = __ldg(p.indptr + r.req);
-  const int pe = __ldg(p.indptr + r.req + 1);
+  const int pb = ptx::ldg_keep(p.indptr + r.req, keep);
+  const int pe = ptx::ldg_keep(p.indptr + r.req + 1, keep);
   long long len = 0;
   if (pe > pb) {
-    const int last = min(max(__ldg(p.last + r.req), 1), p.page_size);
+    const int last = min(max(ptx::ldg_keep(p.last + r.req, keep), 1), p.page_size);
     len = static_cast<long long>(pe - pb - 1) * p.page_size + last;
   }
   if (r.t1 > len) {
@@ -184,7 +185,7 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
       const int tok0 = unit.t0 + t * kTile;
       const int pi = tok0 / p.page_size;
       const int slot0 = tok0 - pi * p.page_size;
-      int page = __ldg(p.indices + unit.pbase + pi);
+      int page = ptx::ldg_keep(p.indices + unit.pbase + pi, ptx::policy_evict_last());
       if (static_cast<unsigned long long>(page) >=
           static_cast<unsigned long long>(p.num_pages)) {
         if (lane == 0) flag(p.image, PKD_DEVICE_BAD_PAGE);
@@ -228,6 +229,7 @@ __device__ void load_bulk(const Params &p, const int32_t *units, int num_partial
   const int lane = threadIdx.x & 31;
   const int tensor = lane >> 4, r = lane & 15;
   const uint16_t *base = tensor ? p.v : p.k;
+  const uint64_t keep = ptx::policy_evict_last();  // page ids stay in L2
   const uint32_t stage0 = ptx::smem_u32(stages);
 
   // cursor over the CTA's tiles; (tok0, t1, page, slot) describe the next one
@@ -252,12 +254,12 @@ __device__ void load_bulk(const Params &p, const int32_t *units, int num_partial
     if (tok < t1) {
       const int pi = tok / p.page_size;
       slot = tok - pi * p.page_size;
-      page = __ldg(p.indices + unit.pbase + pi);
+      page = ptx::ldg_keep(p.indices + unit.pbase + pi, keep);
     }
     if constexpr (kSmallPages) {
       // within this unit only: its page ids are inside the request's range
       const int ahead = tok + kIdPrefetchTiles * kTile;
-      if (ahead < t1) ptx::prefetch_l2(p.indices + unit.pbase + ahead / p.page_size);
+      if (ahead < t1) ptx::prefetch_l2_keep(p.indices + unit.pbase + ahead / p.page_size);
     }
     ++t;
   };
@@ -316,6 +318,7 @@ __device__ void consume(const Params &p, const int32_t *units, int num_partials,
   constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hk = warp / kQw, qpart = warp % kQw;
+  const uint64_t keep = ptx::policy_evict_last();  // queries and states stay in L2
   const int gid = lane >> 2, tq = lane & 3;
   const int gq = (p.group + kQw - 1) / kQw;       // query heads per warp
   const int col_lo = qpart * gq;
@@ -347,9 +350,9 @@ __device__ void consume(const Params &p, const int32_t *units, int num_partials,
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         qb[n][kk][0] =
-            ok ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 2 * tq)) : 0u;
+            ok ? ptx::ldg_keep_u32(qrow + 16 * kk + 2 * tq, keep) : 0u;
         qb[n][kk][1] =
-            ok ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 16 * kk + 8 + 2 * tq)) : 0u;
+            ok ? ptx::ldg_keep_u32(qrow + 16 * kk + 8 + 2 * tq, keep) : 0u;
       }
     }
 
@@ -505,19 +508,19 @@ __device__ void consume(const Params &p, const int32_t *units, int num_partials,
           for (int mt = 0; mt < 8; ++mt) {
             const uint32_t pair =
                 ptx::pack2<T>(acc[n][mt][j] * inv, acc[n][mt][j + 2] * inv);
-            o[16 * mt + gid] = static_cast<uint16_t>(pair & 0xffffu);
-            o[16 * mt + gid + 8] = static_cast<uint16_t>(pair >> 16);
+            ptx::stg_keep_u16(o + 16 * mt + gid, static_cast<uint16_t>(pair & 0xffffu), keep);
+            ptx::stg_keep_u16(o + 16 * mt + gid + 8, static_cast<uint16_t>(pair >> 16), keep);
           }
-          if (gid == 0) p.lse[static_cast<long long>(unit.req) * p.hq + head] = lse_h;
+          if (gid == 0) ptx::stg_keep(p.lse + static_cast<long long>(unit.req) * p.hq + head, lse_h, keep);
         } else {
           float *base = p.partials + static_cast<long long>(unit.slot) * slot_floats;
           float *o = base + head * kHeadDim;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
-            o[16 * mt + gid] = acc[n][mt][j] * inv;
-            o[16 * mt + gid + 8] = acc[n][mt][j + 2] * inv;
+            ptx::stg_keep(o + 16 * mt + gid, acc[n][mt][j] * inv, keep);
+            ptx::stg_keep(o + 16 * mt + gid + 8, acc[n][mt][j + 2] * inv, keep);
           }
-          if (gid == 0) base[p.hq * kHeadDim + head] = lse_h;
+          if (gid == 0) ptx::stg_keep(base + p.hq * kHeadDim + head, lse_h, keep);
         }
       }
   }
@@ -548,10 +551,10 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     if (lane < kHeaderWords) {
-      hdr[lane] = __ldg(img + lane);
+      hdr[lane] = ptx::ldg_keep(img + lane, ptx::policy_evict_last());
     } else if (lane < kHeaderWords + 2) {
       const long long w = kHeaderWords + static_cast<long long>(blockIdx.x) + (lane - kHeaderWords);
-      hdr[lane] = w < p.image_words ? __ldg(img + w) : -1;
+      hdr[lane] = w < p.image_words ? ptx::ldg_keep(img + w, ptx::policy_evict_last()) : -1;
     }
   }
   __syncthreads();

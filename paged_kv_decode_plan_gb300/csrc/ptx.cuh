@@ -128,12 +128,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// Brings the line holding *p into L2 ahead of a later load (no register
-// result, so the issuing thread does not wait for it).
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
-}
-
 // ---- mbarrier (shared::cta, 64-bit) ------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count)
@@ -204,6 +198,46 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       " [%0], [%1], %2, [%3];\n" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// ---- L2 priority for data read again -----------------------------------
+// A decode launch streams several times L2's capacity of K/V through it.
+// The small data that is read again -- within the launch (plan image, page
+// table, queries) or right after it (partial states, by the merge kernel),
+// or by the next step (the page table) -- is loaded and stored with an
+// evict-last L2 policy so that the stream does not push it out.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(policy));
+  return policy;
+}
+
+__device__ __forceinline__ int32_t ldg_keep(const int32_t *p, uint64_t policy) {
+  int32_t v;
+  asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;\n"
+               : "=r"(v) : "l"(p), "l"(policy));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_keep_u32(const void *p, uint64_t policy) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;\n"
+               : "=r"(v) : "l"(p), "l"(policy));
+  return v;
+}
+
+__device__ __forceinline__ void stg_keep(float *p, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(p), "f"(v), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void stg_keep_u16(uint16_t *p, uint16_t v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;\n" ::"l"(p), "h"(v), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2_keep(const void *p) {
+  asm volatile("prefetch.global.L2::evict_last [%0];\n" ::"l"(p));
 }
 
 // ---- movmatrix: transpose of an 8x8 b16 matrix held one pair per lane ---
