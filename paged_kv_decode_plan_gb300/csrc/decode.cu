@@ -170,6 +170,7 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
   constexpr int kStages = G::kStages;
   const int lane = threadIdx.x & 31;
   const uint32_t stage0 = ptx::smem_u32(stages);
+  const uint64_t stream = ptx::policy_evict_first();  // K/V: read once
   int it = 0;
   bool ok = true;
   for (int u = u_begin; u < u_end && ok; ++u) {
@@ -200,11 +201,11 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
         const uint32_t dst = stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
                              head * G::kHeadBytes + half * kHalfBytes;
         if (p.hnd)
-          ptx::tma_load_4d(dst, tensor ? map_v : map_k, half * 64, slot0, head, page,
-                           full0 + 8 * s);
+          ptx::tma_load_4d_hint(dst, tensor ? map_v : map_k, half * 64, slot0, head, page,
+                                full0 + 8 * s, stream);
         else
-          ptx::tma_load_3d(dst, tensor ? map_v : map_k, half * 64, head,
-                           page * p.page_size + slot0, full0 + 8 * s);
+          ptx::tma_load_3d_hint(dst, tensor ? map_v : map_k, half * 64, head,
+                                page * p.page_size + slot0, full0 + 8 * s, stream);
       }
       ++it;
     }
@@ -229,7 +230,8 @@ __device__ void load_bulk(const Params &p, const int32_t *units, int num_partial
   const int lane = threadIdx.x & 31;
   const int tensor = lane >> 4, r = lane & 15;
   const uint16_t *base = tensor ? p.v : p.k;
-  const uint64_t keep = ptx::policy_evict_last();  // page ids stay in L2
+  const uint64_t keep = ptx::policy_evict_last();     // page ids stay in L2
+  const uint64_t stream = ptx::policy_evict_first();  // K/V: read once
   const uint32_t stage0 = ptx::smem_u32(stages);
 
   // cursor over the CTA's tiles; (tok0, t1, page, slot) describe the next one
@@ -288,15 +290,15 @@ __device__ void load_bulk(const Params &p, const int32_t *units, int num_partial
         // HND: the token's head rows are P * 256 bytes apart
 #pragma unroll
         for (int h = 0; h < HKV; ++h)
-          ptx::bulk_load(dst + h * kRowBytes,
-                         base + ((static_cast<long long>(pg) * HKV + h) * p.page_size +
-                                 slot) * kHeadDim,
-                         kRowBytes, full0 + 8 * s);
+          ptx::bulk_load_hint(dst + h * kRowBytes,
+                              base + ((static_cast<long long>(pg) * HKV + h) * p.page_size +
+                                      slot) * kHeadDim,
+                              kRowBytes, full0 + 8 * s, stream);
       } else {
-        ptx::bulk_load(dst,
-                       base + (static_cast<long long>(pg) * p.page_size + slot) * HKV *
-                                  kHeadDim,
-                       kRow, full0 + 8 * s);
+        ptx::bulk_load_hint(dst,
+                            base + (static_cast<long long>(pg) * p.page_size + slot) * HKV *
+                                       kHeadDim,
+                            kRow, full0 + 8 * s, stream);
       }
     }
     describe();

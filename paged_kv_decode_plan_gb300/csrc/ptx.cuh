@@ -200,15 +200,22 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
-// ---- L2 priority for data read again -----------------------------------
-// A decode launch streams several times L2's capacity of K/V through it.
-// The small data that is read again -- within the launch (plan image, page
+// ---- L2 priorities ------------------------------------------------------
+// A decode launch streams several times L2's capacity of K/V through it,
+// each line read once.  The small data that is read again -- within the launch (plan image, page
 // table, queries) or right after it (partial states, by the merge kernel),
 // or by the next step (the page table) -- is loaded and stored with an
 // evict-last L2 policy so that the stream does not push it out.
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t policy;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(policy));
+  return policy;
+}
+
+// The K/V stream itself is read once: its lines go first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(policy));
   return policy;
 }
 
@@ -238,6 +245,37 @@ __device__ __forceinline__ void stg_keep_u16(uint16_t *p, uint16_t v, uint64_t p
 
 __device__ __forceinline__ void prefetch_l2_keep(const void *p) {
   asm volatile("prefetch.global.L2::evict_last [%0];\n" ::"l"(p));
+}
+
+// tma_load_3d / tma_load_4d / bulk_load with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tensor_map, int c0,
+                                                 int c1, int c2, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar),
+      "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *tensor_map, int c0,
+                                                 int c1, int c2, int c3, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void *src, uint32_t bytes,
+                                               uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
 }
 
 // ---- movmatrix: transpose of an 8x8 b16 matrix held one pair per lane ---
