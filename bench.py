@@ -387,6 +387,15 @@ class Runner:
         if self.fused:
             pre, part = self.prefix, self.parts[0]
             ws, plan, final = part["ws"][i], part["plan"], self.finals[i]
+            if events is None:
+                # the single call a user makes (its decode overlaps the prefix
+                # kernel's last CTAs); the timed pass below launches the same
+                # kernels one by one with events between them
+                self.pkd.run_cascade(plan, pre["plan"], self.qs[i], self.k, self.v,
+                                     *part["devs"][i], ws, pre["ws"][i], self.wl.sm_scale,
+                                     out=final[0], lse=final[1])
+                self.launches_per_step = 3
+                return
             if events is not None:
                 events[2].record(main)
             pre["ws"][i].run_states(pre["plan"], self.qs[i], self.k, self.v,

@@ -122,6 +122,65 @@ pkd_status check_cascade(const pkd_plan_t *plan, const pkd_prefix_plan_t *prefix
   return PKD_OK;
 }
 
+// Checks a decode launch and starts the decode kernel (pkd_run_decode; the
+// cascade launches it as a programmatic dependent of the prefix kernel).
+pkd_status launch_decode_checked(const pkd_plan_t *plan, const void *q, const void *k_pages,
+                                 const void *v_pages, const int32_t *kv_indptr_d,
+                                 const int32_t *kv_indices_d,
+                                 const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                                 void *float_ws_dev, size_t float_ws_bytes, float sm_scale,
+                                 void *out, float *lse, void *stream, int programmatic) {
+  if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "plan not valid");
+  const pkd_problem &p = plan->problem;
+  pkd_status st = pkd::check_problem(p, true);
+  if (st != PKD_OK) return st;
+  if (p.batch == 0) return PKD_OK;
+  if (!q || !out || !lse || !kv_indptr_d || !kv_last_page_len_d || !int_ws_dev)
+    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (plan->total_tokens > 0 && (!k_pages || !v_pages || !kv_indices_d))
+    return fail(PKD_ERR_INVALID_ARG, "null page pool or page ids");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      !aligned16(out) || !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
+    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
+  if (plan->num_partials > 0 &&
+      (!float_ws_dev ||
+       float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed)))
+    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the plan needs");
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f))
+    return fail(PKD_ERR_INVALID_ARG, "sm_scale must be finite and positive");
+
+  pkd::DecodeArgs a;
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.kv_indptr = kv_indptr_d;
+  a.kv_indices = kv_indices_d;
+  a.kv_last_page_len = kv_last_page_len_d;
+  a.image = static_cast<int32_t *>(int_ws_dev);
+  a.partials = static_cast<float *>(float_ws_dev);
+  a.out = out;
+  a.lse = lse;
+  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  const Bounds bounds = launch_bounds(*plan, float_ws_bytes, capturing(stream));
+  a.num_pages = p.num_pages;
+  a.batch = bounds.batch;
+  a.num_qo_heads = p.num_qo_heads;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  a.num_ctas = p.num_ctas;
+  a.dtype = p.dtype;
+  a.max_partials = bounds.max_partials;
+  a.image_words = bounds.image_words;
+  a.loader = p.kv_loader;
+  a.layout = p.kv_layout;
+  a.programmatic = programmatic;
+  cudaError_t e = static_cast<cudaError_t>(pkd::launch_decode(a, stream));
+  if (e == cudaErrorNotSupported)
+    return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");
+  if (e != cudaSuccess) return cuda_fail(e, "launching the decode kernel");
+  return PKD_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -188,54 +247,9 @@ pkd_status pkd_run_decode(const pkd_plan_t *plan, const void *q,
                           void *float_ws_dev, size_t float_ws_bytes,
                           float sm_scale, void *out, float *lse, void *stream) {
   pkd::clear_error();
-  if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "plan not valid");
-  const pkd_problem &p = plan->problem;
-  pkd_status st = pkd::check_problem(p, true);
-  if (st != PKD_OK) return st;
-  if (p.batch == 0) return PKD_OK;
-  if (!q || !out || !lse || !kv_indptr_d || !kv_last_page_len_d || !int_ws_dev)
-    return fail(PKD_ERR_INVALID_ARG, "null device pointer");
-  if (plan->total_tokens > 0 && (!k_pages || !v_pages || !kv_indices_d))
-    return fail(PKD_ERR_INVALID_ARG, "null page pool or page ids");
-  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) ||
-      !aligned16(out) || !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
-    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
-  if (plan->num_partials > 0 &&
-      (!float_ws_dev ||
-       float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed)))
-    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the plan needs");
-  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f))
-    return fail(PKD_ERR_INVALID_ARG, "sm_scale must be finite and positive");
-
-  pkd::DecodeArgs a;
-  a.q = q;
-  a.k_pages = k_pages;
-  a.v_pages = v_pages;
-  a.kv_indptr = kv_indptr_d;
-  a.kv_indices = kv_indices_d;
-  a.kv_last_page_len = kv_last_page_len_d;
-  a.image = static_cast<int32_t *>(int_ws_dev);
-  a.partials = static_cast<float *>(float_ws_dev);
-  a.out = out;
-  a.lse = lse;
-  a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-  const Bounds bounds = launch_bounds(*plan, float_ws_bytes, capturing(stream));
-  a.num_pages = p.num_pages;
-  a.batch = bounds.batch;
-  a.num_qo_heads = p.num_qo_heads;
-  a.num_kv_heads = p.num_kv_heads;
-  a.page_size = p.page_size;
-  a.num_ctas = p.num_ctas;
-  a.dtype = p.dtype;
-  a.max_partials = bounds.max_partials;
-  a.image_words = bounds.image_words;
-  a.loader = p.kv_loader;
-  a.layout = p.kv_layout;
-  cudaError_t e = static_cast<cudaError_t>(pkd::launch_decode(a, stream));
-  if (e == cudaErrorNotSupported)
-    return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");
-  if (e != cudaSuccess) return cuda_fail(e, "launching the decode kernel");
-  return PKD_OK;
+  return launch_decode_checked(plan, q, k_pages, v_pages, kv_indptr_d, kv_indices_d,
+                               kv_last_page_len_d, int_ws_dev, float_ws_dev, float_ws_bytes,
+                               sm_scale, out, lse, stream, 0);
 }
 
 pkd_status pkd_run_merge(const pkd_plan_t *plan, const void *int_ws_dev,
@@ -495,9 +509,11 @@ pkd_status pkd_run_cascade(const pkd_plan_t *plan, const void *q, const void *k_
   st = start_prefix(prefix_plan, q, k_pages, v_pages, prefix_int_ws_dev,
                     prefix_float_ws_dev, prefix_float_ws_bytes, sm_scale, stream);
   if (st != PKD_OK) return st;
-  st = pkd_run_decode(plan, q, k_pages, v_pages, kv_indptr_d, kv_indices_d,
-                      kv_last_page_len_d, int_ws_dev, float_ws_dev, float_ws_bytes,
-                      sm_scale, out, lse, stream);
+  // the suffix decode reads nothing the prefix kernel writes: it may start as
+  // the prefix kernel's CTAs retire (and waits for that grid before exiting)
+  st = launch_decode_checked(plan, q, k_pages, v_pages, kv_indptr_d, kv_indices_d,
+                             kv_last_page_len_d, int_ws_dev, float_ws_dev, float_ws_bytes,
+                             sm_scale, out, lse, stream, 1);
   if (st != PKD_OK) return st;
   return pkd_run_cascade_merge(plan, int_ws_dev, float_ws_dev, float_ws_bytes, prefix_plan,
                                prefix_int_ws_dev, prefix_float_ws_dev,

@@ -98,6 +98,7 @@ struct Params {
   int image_words;    // int32 words the image may span
   int grid;           // CTAs launched
   int hnd;            // page tensors are HND
+  int programmatic;   // launched as a programmatic dependent (host side only)
   // batch: requests the q / out / lse / page-table buffers hold; a plan may
   // cover fewer (a captured launch replayed with a later, smaller plan)
 };
@@ -571,6 +572,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
       num_partials > p.max_partials || hdr[kHNumSplit] < 0 ||
       image_offsets(num_ctas, num_units, hdr[kHNumSplit]).end > p.image_words) {
     if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
+    ptx::wait_primary_grid();
     return;
   }
   const int32_t *units = img + kHeaderWords + num_ctas + 1;
@@ -579,12 +581,21 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
   q.batch = hdr[kHBatch];  // this plan's batch (p.batch is the buffers' capacity)
   if (u_begin < 0 || u_end > num_units || u_begin > u_end) {
     if (threadIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
+    ptx::wait_primary_grid();
     return;
   }
   // a merge kernel launched after this one may be scheduled from now on; it
   // waits for this grid to finish before it reads any partial state
   ptx::launch_dependents();
-  if (u_begin == u_end) return;
+  // Launched as a programmatic dependent (the cascade's suffix decode after
+  // the shared-prefix kernel), this grid reads nothing the grid before it
+  // writes, but every thread waits for that grid before exiting, so that a
+  // kernel waiting for this grid's completion also sees the earlier grid's
+  // results.  In a normal launch the wait returns at once.
+  if (u_begin == u_end) {
+    ptx::wait_primary_grid();
+    return;
+  }
 
   if (threadIdx.x == 0) {
     const uint32_t full_count = 1u;  // the loader's arrive.expect_tx
@@ -612,6 +623,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
     consume<T, HKV, NG, LOADER>(q, units, num_partials, u_begin, u_end, stages, full0,
                                 empty0, abort);
   }
+  ptx::wait_primary_grid();
 }
 
 constexpr int kMaxDevices = 64;
@@ -632,8 +644,24 @@ int launch_typed(const Params &prm, const CUtensorMap &mk, const CUtensorMap &mv
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) raised[dev].store(true, std::memory_order_release);
   }
-  kernel<<<prm.grid, 32 * (kConsumerWarps + G::kLoaderWarps), smem,
-           static_cast<cudaStream_t>(stream)>>>(prm, mk, mv);
+  if (prm.programmatic) {
+    // may start while the kernel before it on the stream still runs
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(prm.grid);
+    cfg.blockDim = dim3(32 * (kConsumerWarps + G::kLoaderWarps));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, prm, mk, mv);
+    if (e != cudaSuccess) return e;
+  } else {
+    kernel<<<prm.grid, 32 * (kConsumerWarps + G::kLoaderWarps), smem,
+             static_cast<cudaStream_t>(stream)>>>(prm, mk, mv);
+  }
   return cudaGetLastError();
 }
 
@@ -795,6 +823,7 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   prm.image_words = a.image_words;
   prm.grid = a.num_ctas;
   prm.hnd = a.layout == PKD_LAYOUT_HND;
+  prm.programmatic = a.programmatic;
 
   CUtensorMap mk;
   CUtensorMap mv;

@@ -95,6 +95,7 @@ struct DecodeArgs {
   int max_partials, image_words;
   int loader;  // pkd_loader of the problem
   int layout;  // pkd_layout of the page tensors
+  int programmatic;  // launch as a programmatic dependent of the previous kernel
 };
 int launch_decode(const DecodeArgs &a, void *stream);
 
