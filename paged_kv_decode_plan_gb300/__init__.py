@@ -89,7 +89,9 @@ def load():
         raise RuntimeError(
             "libpkd.so is not built: run `python -m paged_kv_decode_plan_gb300.build`")
     lib = ctypes.CDLL(LIB_PATH)
-    vp, i32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)
+    # host int32 arrays are passed as plain addresses (numpy's .ctypes view
+    # costs microseconds per array, more than the planner itself)
+    vp = i32p = ctypes.c_void_p
     sz = ctypes.POINTER(ctypes.c_size_t)
     lib.pkd_abi_version.restype = ctypes.c_int32
     lib.pkd_last_error.restype = ctypes.c_char_p
@@ -179,7 +181,15 @@ def _host_i32(x):
     a = np.ascontiguousarray(x, dtype=np.int32)
     if a.size == 0:
         a = np.zeros(1, dtype=np.int32)
-    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    return a, _addr(a)
+
+
+def _addr(a):
+    """Address of a numpy array's first element (the caller keeps ``a`` alive);
+    the buffer protocol is several times cheaper than numpy's ctypes view."""
+    if a.flags.writeable:
+        return ctypes.addressof(ctypes.c_char.from_buffer(a))
+    return a.ctypes.data
 
 
 def plan_host(problem: Problem, kv_indptr, kv_last_page_len, kv_indices=None):
@@ -195,7 +205,7 @@ def plan_host(problem: Problem, kv_indptr, kv_last_page_len, kv_indices=None):
     out = Plan()
     _check(load().pkd_plan_host(ctypes.byref(prob), p_indptr, p_last, p_idx,
                                 ctypes.byref(out),
-                                image.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                _addr(image),
                                 image.nbytes))
     return out, image[: out.int_ws_bytes_used // 4].copy()
 
@@ -204,11 +214,13 @@ def _stream_ptr(stream):
     import torch
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # every entry point declares its pointer arguments c_void_p, so a plain
+    # int is passed as a full-width address
+    return None if t is None else t.data_ptr()
 
 
 def plan(problem: Problem, kv_indptr, kv_last_page_len, kv_indices=None, *,
@@ -282,7 +294,7 @@ def run_static(plan_: Plan, host_image, q, k_pages, v_pages, kv_indptr, kv_indic
                           device=q.device)
     image = np.ascontiguousarray(host_image, dtype=np.int32)
     _check(load().pkd_run_static(
-        ctypes.byref(plan_), image.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        ctypes.byref(plan_), _addr(image),
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_indptr), _ptr(kv_indices),
         _ptr(kv_last_page_len), float(sm_scale), _ptr(out), _ptr(lse),
         _stream_ptr(stream)))

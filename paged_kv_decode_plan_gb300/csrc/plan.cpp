@@ -104,7 +104,9 @@ pkd_status plan_host_impl(const pkd_problem &in, const int32_t *kv_indptr,
   if (p.tile_tokens == 0) p.tile_tokens = kTileTokens;
   pkd_status st = check_problem(p, true);
   if (st != PKD_OK) return st;
-  const int B = p.batch, P = p.page_size, T = p.tile_tokens, C = p.num_ctas;
+  // tile_tokens is 0 or kTileTokens (check_problem): a compile-time divisor
+  constexpr int T = kTileTokens;
+  const int B = p.batch, P = p.page_size, C = p.num_ctas;
   const int m = std::max(1, p.min_chunks_per_request);
 
   // 1. validate the CSR table, compute lengths and tiles
@@ -158,6 +160,7 @@ pkd_status plan_host_impl(const pkd_problem &in, const int32_t *kv_indptr,
   const int64_t quota = std::max<int64_t>(1, (total_tiles + C - 1) / C);
   struct Unit { int32_t req, t0, t1, slot; };
   std::vector<Unit> units;
+  units.reserve(static_cast<size_t>(std::min<int64_t>(max_units(p), total_tiles + B + C)));
   std::vector<int32_t> cta_ptr;
   cta_ptr.reserve(C + 1);
   cta_ptr.push_back(0);
@@ -178,7 +181,8 @@ pkd_status plan_host_impl(const pkd_problem &in, const int32_t *kv_indptr,
         used = 0;
       }
       const int64_t room = cta < C - 1 ? quota - used : n - pos;
-      const int64_t take = std::min(std::min(n - pos, cap - pos % cap), room);
+      const int64_t to_cap = m <= 1 ? n - pos : cap - pos % cap;
+      const int64_t take = std::min(std::min(n - pos, to_cap), room);
       units.push_back({b, static_cast<int32_t>(pos * T),
                        static_cast<int32_t>(std::min((pos + take) * T, length[b])),
                        -1});
