@@ -236,8 +236,10 @@ class Runner:
         self.pkd = pkd
         self.wl = wl
         self.device = device
-        self.q = wl.q.to(device)
-        self.qs = [self.q, self.q.clone()]
+        # every workspace turn holds its queries and packed page tables in one
+        # device buffer (one host-to-device copy per step end to end); each
+        # output pair (out, lse) likewise sits in one buffer (one read-back)
+        self.q_bytes = wl.q.numel() * wl.q.element_size()
         self.k = wl.k_pages.to(device)
         self.v = wl.v_pages.to(device)
         self.layout = pkd.LAYOUT_HND if layout == "hnd" else pkd.LAYOUT_NHD
@@ -257,6 +259,14 @@ class Runner:
             self.tables = [wl.extra_tables["suffix"]]
         else:
             self.tables = [wl.table]
+        packed_tables = [pack_table(t) for t in self.tables]
+        self.in_offsets, in_bytes = _layout([self.q_bytes] + [pk.nbytes for pk in packed_tables])
+        self.inbufs = [torch.empty(in_bytes, dtype=torch.uint8, device=device)
+                       for _ in range(2)]
+        self.qs = [buf[:self.q_bytes].view(wl.q.dtype).view(wl.q.shape) for buf in self.inbufs]
+        for qd in self.qs:
+            qd.copy_(wl.q)
+        self.q = self.qs[0]
         self.prefix = None
         if self.shared:
             pt = wl.extra_tables["prefix"]
@@ -268,32 +278,33 @@ class Runner:
             self.prefix = dict(
                 pages=pages, last=int(pt.kv_last_page_len[0]),
                 ws=[pkd.PrefixWorkspace(prob, pages.size, device=device) for _ in range(2)],
-                outs=[(torch.empty_like(self.q),
-                       torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
-                      for _ in range(2)])
+                outs=[self._pair() for _ in range(2)])
         self.parts = []
-        for t in self.tables:
+        for n, t in enumerate(self.tables):
             prob = pkd.make_problem(batch=t.batch, num_qo_heads=wl.num_qo_heads,
                                     num_kv_heads=wl.num_kv_heads, page_size=t.page_size,
                                     dtype=wl.dtype, num_pages=wl.num_pages,
                                     min_chunks_per_request=wl.min_chunks_per_request,
                                     kv_loader=kv_loader, kv_layout=self.layout)
             ws = [pkd.Workspace(prob, device=device) for _ in range(2)]
-            # the three page-table arrays packed in one buffer per turn (one
-            # host-to-device copy per step); the API gets views into it
-            packed = pack_table(t)
+            # the three page-table arrays packed together after the queries in
+            # the turn's input buffer; the API gets views into it
+            packed = packed_tables[n]
             n0, n1 = t.kv_indptr.size, t.kv_indices.size
-            packs = [torch.from_numpy(packed).to(device) for _ in range(2)]
+            off = self.in_offsets[1 + n]
+            packs = [buf[off:off + packed.nbytes].view(torch.int32) for buf in self.inbufs]
+            for pk in packs:
+                pk.copy_(torch.from_numpy(packed))
             devs = [(pk[:n0], pk[n0:n0 + n1], pk[n0 + n1:]) for pk in packs]
-            outs = [(torch.empty_like(self.q),
-                     torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
-                    for _ in range(2)]
+            outs = [self._pair() for _ in range(2)]
             self.parts.append(dict(table=t, ws=ws, devs=devs, packs=packs, outs=outs))
-        self.finals = [(torch.empty_like(self.q),
-                        torch.empty(self.q.shape[:2], dtype=torch.float32, device=device))
-                       for _ in range(2)]
+        self.finals = [self._pair() for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(device)
         self.read_stream = torch.cuda.Stream(device)
+        # per-turn events, created once and re-recorded every step
+        self.ready_ev = [torch.cuda.Event(), torch.cuda.Event()]
+        self.done_ev = [torch.cuda.Event(), torch.cuda.Event()]
+        self.read_ev = [torch.cuda.Event(), torch.cuda.Event()]
         self.done = [None, None]
         self.read = [None, None]   # read-back of a turn's outputs (end to end)
         self.last_turn = 0
@@ -311,10 +322,25 @@ class Runner:
             self.timing_events = None
         self.timings = []   # (decode_ms, prefix_ms) of timed graph steps
 
+    def _pair(self):
+        """(out, lse, buffer): one output pair as views into one device buffer."""
+        torch = self.torch
+        lse_bytes = self.q.shape[0] * self.q.shape[1] * 4
+        offs, total = _layout([self.q_bytes, lse_bytes])
+        buf = torch.empty(total, dtype=torch.uint8, device=self.device)
+        out = buf[:self.q_bytes].view(self.q.dtype).view(self.q.shape)
+        lse = buf[offs[1]:offs[1] + lse_bytes].view(torch.float32).view(self.q.shape[:2])
+        return out, lse, buf
+
+    def host_inputs(self):
+        """A pinned copy of a turn's input buffer (queries, packed tables)."""
+        return self.inbufs[0].cpu().pin_memory()
+
     def step(self, events=None, inputs=None, outputs=None):
-        """One step on workspace turn i.  ``inputs`` = (pinned q, pinned packed
-        page table per part) are copied in on the copy stream; ``outputs`` =
-        pinned (out, lse) receive the step's result on the read-back stream."""
+        """One step on workspace turn i.  ``inputs`` (a pinned copy of the input
+        buffer: queries and packed page tables) is copied in on the copy stream;
+        ``outputs`` (a pinned buffer the size of a result pair's) receives the
+        step's (out, lse) on the read-back stream."""
         torch = self.torch
         main = torch.cuda.current_stream()
         i = self.turn
@@ -323,11 +349,8 @@ class Runner:
         if self.done[i] is not None:
             self.copy_stream.wait_event(self.done[i])
         if inputs is not None:
-            q_h, tables_h = inputs
             with torch.cuda.stream(self.copy_stream):
-                self.qs[i].copy_(q_h, non_blocking=True)
-                for part, th in zip(self.parts, tables_h):
-                    part["packs"][i].copy_(th, non_blocking=True)
+                self.inbufs[i].copy_(inputs, non_blocking=True)
         for part in self.parts:
             t = part["table"]
             part["plan"] = part["ws"][i].plan(t.kv_indptr, t.kv_last_page_len, None,
@@ -336,7 +359,7 @@ class Runner:
             pre = self.prefix
             pre["plan"] = pre["ws"][i].plan(pre["pages"], pre["last"],
                                             stream=self.copy_stream)
-        ready = torch.cuda.Event()
+        ready = self.ready_ev[i]
         ready.record(self.copy_stream)
         main.wait_event(ready)
         if self.read[i] is not None:   # this turn's previous outputs were read back
@@ -354,16 +377,15 @@ class Runner:
         else:
             self._launch(i, events)
             self.eager_steps += 1
-        done = torch.cuda.Event()
+        done = self.done_ev[i]
         done.record(main)
         self.done[i] = done
         if outputs is not None:
             res = self.result()
             self.read_stream.wait_event(done)
             with torch.cuda.stream(self.read_stream):
-                outputs[0].copy_(res[0], non_blocking=True)
-                outputs[1].copy_(res[1], non_blocking=True)
-            rd = torch.cuda.Event()
+                outputs.copy_(res[2], non_blocking=True)
+            rd = self.read_ev[i]
             rd.record(self.read_stream)
             self.read[i] = rd
 
@@ -510,6 +532,16 @@ class Runner:
         return int(self.tables[0].lengths().sum()) * per_token
 
 
+def _layout(sizes, align=256):
+    """(offsets, total) of byte ranges packed one after another, each start
+    aligned to ``align`` bytes."""
+    offs, off = [], 0
+    for n in sizes:
+        offs.append(off)
+        off += (n + align - 1) // align * align
+    return offs, off
+
+
 def pack_table(t):
     """indptr, indices and last_page_len of a page table in one int32 array."""
     return np.concatenate([t.kv_indptr, t.kv_indices, t.kv_last_page_len]).astype(np.int32)
@@ -554,6 +586,9 @@ def run_ours(args, ranks):
     status = runner.status()
     if status:
         raise RuntimeError("device status word %d after warm-up" % status)
+    out, lse, _ = runner.result()
+    if not bool(torch.isfinite(out).all()) or bool(torch.isnan(lse).any()):
+        raise RuntimeError("non-finite output after warm-up")
 
     uuid = None
     try:
@@ -663,20 +698,18 @@ def run_e2e(args, runner, device, ranks):
     with a synchronise after the last read-back."""
     import torch
     wl = runner.wl
-    q_h = wl.q.pin_memory()
-    tables_h = [torch.from_numpy(pack_table(p["table"])).pin_memory() for p in runner.parts]
-    outs_h = [(torch.empty(runner.q.shape, dtype=runner.q.dtype, pin_memory=True),
-               torch.empty(runner.q.shape[:2], dtype=torch.float32, pin_memory=True))
-              for _ in range(2)]
-    h2d = q_h.numel() * q_h.element_size() + sum(th.numel() * 4 for th in tables_h)
-    d2h = outs_h[0][0].numel() * outs_h[0][0].element_size() + outs_h[0][1].numel() * 4
+    in_h = runner.host_inputs()
+    res_bytes = runner.result()[2].numel()
+    outs_h = [torch.empty(res_bytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    h2d = in_h.numel()
+    d2h = res_bytes
     steps = max(3, min(args.steps, args.e2e_steps))
     turn = [0]
 
     def one():
         i = turn[0]
         turn[0] ^= 1
-        runner.step(inputs=(q_h, tables_h), outputs=outs_h[i])
+        runner.step(inputs=in_h, outputs=outs_h[i])
 
     for _ in range(3):
         one()
@@ -689,6 +722,9 @@ def run_e2e(args, runner, device, ranks):
         one()
     torch.cuda.synchronize()
     elapsed = time.perf_counter() - t0
+    # the last read-back holds the last step's device result
+    if not torch.equal(outs_h[turn[0] ^ 1], runner.result()[2].cpu()):
+        raise RuntimeError("read-back differs from the device result")
     agg = aggregate(ranks, runner.kv_bytes(), elapsed, steps)
     return {"value": round(agg["value_gbs"], 2), "unit": "GB/s",
             "us_per_batch": round(agg["ms_per_step"] * 1e3, 2), "steps": steps,

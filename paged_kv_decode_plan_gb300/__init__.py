@@ -469,19 +469,21 @@ class PrefixWorkspace:
         self.int_ws = torch.zeros(ib, dtype=torch.uint8, device=device)
         self.float_ws = torch.empty(max(fb, 16), dtype=torch.uint8, device=device)
         self.staging = torch.empty(sb // 4 + 4, dtype=torch.int32, pin_memory=True)
-        self.event = None
+        self.event = torch.cuda.Event()   # re-recorded after every image copy
+        self.recorded = False
 
     def plan(self, prefix_pages, prefix_last_page_len, *, batch=None, stream=None):
         import torch
-        prob = Problem.from_buffer_copy(self.problem)
+        prob = self.problem
         if batch is not None:
+            prob = Problem.from_buffer_copy(self.problem)
             prob.batch = batch
-        if self.event is not None:
+        if self.recorded:
             self.event.synchronize()
         out = plan_shared_prefix(prob, prefix_pages, prefix_last_page_len,
                                  staging=self.staging, int_ws=self.int_ws, stream=stream)
-        self.event = torch.cuda.Event()
         self.event.record(stream or torch.cuda.current_stream())
+        self.recorded = True
         return out
 
     def run(self, plan_: PrefixPlan, q, k_pages, v_pages, sm_scale, out=None, lse=None,
@@ -511,23 +513,25 @@ class Workspace:
         self.float_ws = torch.empty(max(fb, 16), dtype=torch.uint8, device=device)
         self.staging = [torch.empty(sb // 4 + 4, dtype=torch.int32, pin_memory=True)
                         for _ in range(2)]
-        self.events = [None, None]
+        # one event per staging buffer, re-recorded after each of its copies
+        self.events = [torch.cuda.Event(), torch.cuda.Event()]
+        self.recorded = [False, False]
         self.turn = 0
 
     def plan(self, kv_indptr, kv_last_page_len, kv_indices=None, *, batch=None,
              stream=None) -> Plan:
         import torch
-        prob = Problem.from_buffer_copy(self.problem)
+        prob = self.problem
         if batch is not None:
+            prob = Problem.from_buffer_copy(self.problem)
             prob.batch = batch
         i = self.turn
-        if self.events[i] is not None:
+        if self.recorded[i]:
             self.events[i].synchronize()
         out = plan(prob, kv_indptr, kv_last_page_len, kv_indices,
                    staging=self.staging[i], int_ws=self.int_ws, stream=stream)
-        ev = torch.cuda.Event()
-        ev.record(stream or torch.cuda.current_stream())
-        self.events[i] = ev
+        self.events[i].record(stream or torch.cuda.current_stream())
+        self.recorded[i] = True
         self.turn ^= 1
         return out
 
