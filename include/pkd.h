@@ -373,7 +373,11 @@ pkd_status pkd_run_shared_prefix_states(const pkd_prefix_plan_t *plan, const voi
  * `stream`: the shared-prefix kernel (chunk states into
  * prefix_float_ws_dev), the decode kernel of pkd_run_decode (unsplit rows'
  * suffix states into out / lse, split rows' partial states into
- * float_ws_dev), then pkd_run_cascade_merge.  out [batch][Hq][D] and lse
+ * float_ws_dev), then pkd_run_cascade_merge.  The decode kernel reads nothing
+ * the prefix kernel writes, so it is launched as a programmatic dependent of
+ * it (its CTAs may start while the prefix kernel's last CTAs run) and waits
+ * for the prefix grid before exiting; the merge, ordered after the decode
+ * grid, therefore sees both kernels' states.  out [batch][Hq][D] and lse
  * [batch][Hq] receive the final states; a request with no tokens at all gets
  * (0, -inf).  No separate prefix out / lse and no pkd_merge_states pass: the
  * prefix states stay fp32 until the final merge.  Workspaces: each plan's

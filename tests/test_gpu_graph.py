@@ -90,3 +90,75 @@ def test_captured_run_follows_later_plans(dtype, loader):
         gh.compare(out[: t.batch], lse[: t.batch], ref_out, ref_lse, dtype)
         if t is cases[-1]:
             assert p.num_split_requests == 0
+
+
+def test_zero_requests():
+    """A plan of no requests launches nothing eagerly and turns a captured
+    decode + merge into a no-op; the graph then follows a non-empty plan."""
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device")
+    dtype = "f16"
+    base = _pool(dtype, 41)
+    dev = gh.DeviceBatch(base)
+    empty = _table([], 5)
+
+    # eager: PKD_OK, outputs untouched
+    prob0 = pkd.make_problem(batch=0, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                             dtype=dtype, num_pages=POOL, num_ctas=24)
+    ws0 = pkd.Workspace(prob0)
+    plan0 = ws0.plan(empty.kv_indptr, empty.kv_last_page_len, empty.kv_indices)
+    assert plan0.num_units == 0 and plan0.num_partials == 0
+    out = torch.full_like(dev.q, 7.0)
+    lse = torch.full(dev.q.shape[:2], 7.0, dtype=torch.float32, device="cuda")
+    indptr0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws0.run(plan0, dev.q, dev.k, dev.v, indptr0, None, indptr0, base.sm_scale,
+            out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()) and bool((lse == 7.0).all())
+
+    # captured on a non-empty plan, replayed after an empty one, then a full one
+    prob = pkd.make_problem(batch=MAX_BATCH, num_qo_heads=32, num_kv_heads=8,
+                            page_size=16, dtype=dtype, num_pages=POOL, num_ctas=24,
+                            max_batch=MAX_BATCH)
+    ws = pkd.Workspace(prob)
+    indptr_d = torch.zeros(MAX_BATCH + 1, dtype=torch.int32, device="cuda")
+    indices_d = torch.zeros(POOL, dtype=torch.int32, device="cuda")
+    last_d = torch.zeros(MAX_BATCH, dtype=torch.int32, device="cuda")
+
+    def load_table(t):
+        indptr_d.zero_()
+        last_d.zero_()
+        indptr_d[: t.batch + 1].copy_(torch.from_numpy(t.kv_indptr))
+        indices_d[: t.kv_indices.size].copy_(torch.from_numpy(t.kv_indices))
+        last_d[: t.batch].copy_(torch.from_numpy(t.kv_last_page_len))
+
+    full = _table([900, 40, 1300, 7, 260, 2100], 6)
+    load_table(full)
+    plan = ws.plan(full.kv_indptr, full.kv_last_page_len, full.kv_indices)
+    assert plan.num_split_requests > 0
+    ws.run(plan, dev.q, dev.k, dev.v, indptr_d, indices_d, last_d, base.sm_scale,
+           out=out, lse=lse)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ws.run(plan, dev.q, dev.k, dev.v, indptr_d, indices_d, last_d, base.sm_scale,
+               out=out, lse=lse)
+
+    load_table(empty)
+    ws.plan(empty.kv_indptr, empty.kv_last_page_len, empty.kv_indices, batch=0)
+    out.fill_(7.0)
+    lse.fill_(7.0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert pkd.check_status(ws.int_ws) == 0
+    assert bool((out == 7.0).all()) and bool((lse == 7.0).all())
+
+    load_table(full)
+    ws.plan(full.kv_indptr, full.kv_last_page_len, full.kv_indices, batch=full.batch)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert pkd.check_status(ws.int_ws) == 0
+    wl = workloads.PagedBatch("graph", 32, 8, 128, dtype, base.q[: full.batch],
+                              base.k_pages, base.v_pages, full, base.sm_scale)
+    ref_out, ref_lse = gh.oracle_ref(wl)
+    gh.compare(out[: full.batch], lse[: full.batch], ref_out, ref_lse, dtype)
