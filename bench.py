@@ -426,7 +426,7 @@ class Runner:
                 events[3].record(main)
                 events[0].record(main)
             ws.run(plan, self.qs[i], self.k, self.v, *part["devs"][i], self.wl.sm_scale,
-                   out=final[0], lse=final[1], phase="decode")
+                   phase="decode_states")
             if events is not None:
                 events[1].record(main)
             self.pkd.run_cascade_merge(plan, pre["plan"], ws, pre["ws"][i], final[0],
@@ -509,9 +509,13 @@ class Runner:
             prefix_states = wl.batch * pre["plan"].chunks * slot
             total += 4 * int(pre["pages"].size) + 4 * int(part["table"].kv_indices.size)
             total += 2 * rows * wl.head_dim * elem          # q read by both kernels
-            total += state + 2 * part["plan"].num_partials * slot   # suffix decode
+            # suffix decode: every request's state fp32 (split requests' partial
+            # slots, one slot per unsplit request), written and read by the merge
+            plan = part["plan"]
+            suffix_slots = plan.num_partials + wl.batch - plan.num_split_requests
+            total += 2 * suffix_slots * slot
             total += 2 * prefix_states                       # prefix states out and in
-            total += 2 * state                               # merge: suffix state in, final out
+            total += state                                   # merge: final out / lse
             return total
         for part in self.parts:
             total += 4 * int(part["table"].kv_indices.size)

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define PKD_ABI_VERSION 3
+#define PKD_ABI_VERSION 4
 
 typedef enum {
   PKD_OK = 0,
@@ -128,7 +128,10 @@ const char *pkd_last_error(void);
  * Workspace sizes for a problem's capacity (max_batch, num_ctas,
  * min_chunks_per_request), valid for every plan of that capacity:
  *   int_ws_bytes   device buffer holding the plan image (int32 words);
- *   float_ws_bytes device buffer for fp32 partial states;
+ *   float_ws_bytes device buffer for fp32 partial states: a slot per work
+ *                  unit the capacity allows plus one per request (the
+ *                  states-only decode of pkd_run_decode_states and the
+ *                  cascade keep every request's state in fp32);
  *   staging_bytes  pinned host buffer pkd_plan() builds the image in.
  * num_ctas == 0 queries the current device.  Any output pointer may be NULL.
  */
@@ -215,6 +218,27 @@ pkd_status pkd_run_decode(const pkd_plan_t *plan, const void *q,
 pkd_status pkd_run_merge(const pkd_plan_t *plan, const void *int_ws_dev,
                          const void *float_ws_dev, size_t float_ws_bytes,
                          void *out, float *lse, void *stream);
+
+/*
+ * The decode kernel in its states-only mode ([W] "Attention states"): every
+ * request's attention state stays fp32 in float_ws_dev and nothing is written
+ * to an out / lse in the input type.  A request the plan split leaves its
+ * partial states in its plan slots (as pkd_run_decode); an unsplit request b,
+ * an empty one included, leaves its state in slot plan->num_partials + b
+ * (o [Hq][head_dim] then lse [Hq], padded to 4 floats; (0, -inf) when empty).
+ * float_ws_bytes must hold plan->num_partials + batch slots
+ * (pkd_workspace_size's float size always does), else PKD_ERR_WORKSPACE.
+ * Other arguments, errors and graph capture as pkd_run_decode; a replay whose
+ * plan needs more slots than float_ws_bytes holds is skipped with
+ * PKD_DEVICE_BAD_PLAN in the status word.  pkd_run_cascade_merge consumes
+ * these states.
+ */
+pkd_status pkd_run_decode_states(const pkd_plan_t *plan, const void *q,
+                                 const void *k_pages, const void *v_pages,
+                                 const int32_t *kv_indptr_d, const int32_t *kv_indices_d,
+                                 const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                                 void *float_ws_dev, size_t float_ws_bytes, float sm_scale,
+                                 void *stream);
 
 /*
  * Merge of two attention states over disjoint regions into the state of
@@ -371,9 +395,10 @@ pkd_status pkd_run_shared_prefix_states(const pkd_prefix_plan_t *plan, const voi
  * dtype, page_size, num_pages and kv_layout (else PKD_ERR_INVALID_ARG, no
  * launch), and one q / k_pages / v_pages serves both.  Launches, on
  * `stream`: the shared-prefix kernel (chunk states into
- * prefix_float_ws_dev), the decode kernel of pkd_run_decode (unsplit rows'
- * suffix states into out / lse, split rows' partial states into
- * float_ws_dev), then pkd_run_cascade_merge.  The decode kernel reads nothing
+ * prefix_float_ws_dev), the decode kernel of pkd_run_decode_states (every
+ * request's suffix state fp32 in float_ws_dev, which must hold
+ * plan->num_partials + batch slots), then pkd_run_cascade_merge, which rounds
+ * each final state to the output type once.  The decode kernel reads nothing
  * the prefix kernel writes, so it is launched as a programmatic dependent of
  * it (its CTAs may start while the prefix kernel's last CTAs run) and waits
  * for the prefix grid before exiting; the merge, ordered after the decode
@@ -398,12 +423,13 @@ pkd_status pkd_run_cascade(const pkd_plan_t *plan, const void *q, const void *k_
 
 /* The last launch of pkd_run_cascade, for callers that launch the prefix
  * states (pkd_run_shared_prefix_states) and the suffix decode
- * (pkd_run_decode into out / lse) themselves, in that order on `stream`,
- * immediately before this call.  Per (request b, query head h) row it folds
- * the prefix chunk states with the suffix state (the request's partial
- * states if its suffix plan split it, else the out / lse row) and writes the
- * result over out / lse.  Launched as a programmatic dependent of the decode
- * kernel. */
+ * (pkd_run_decode_states) themselves, in that order on `stream`, immediately
+ * before this call.  Per (request b, query head h) row it folds the prefix
+ * chunk states with the fp32 suffix state (the request's partial states if
+ * its suffix plan split it, else slot plan->num_partials + b) and writes the
+ * result, rounded once, to out / lse.  float_ws_bytes must hold
+ * plan->num_partials + batch slots (PKD_ERR_WORKSPACE).  Launched as a
+ * programmatic dependent of the decode kernel. */
 pkd_status pkd_run_cascade_merge(const pkd_plan_t *plan, void *int_ws_dev,
                                  const void *float_ws_dev, size_t float_ws_bytes,
                                  const pkd_prefix_plan_t *prefix_plan,

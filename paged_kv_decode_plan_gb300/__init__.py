@@ -31,7 +31,7 @@ STATUS_NAMES = {0: "PKD_OK", -1: "PKD_ERR_INVALID_ARG", -2: "PKD_ERR_PAGE_TABLE"
                 -3: "PKD_ERR_WORKSPACE", -4: "PKD_ERR_UNSUPPORTED",
                 -5: "PKD_ERR_CUDA", -6: "PKD_ERR_DEVICE_CHECK"}
 
-ABI_VERSION = 3  # PKD_ABI_VERSION of include/pkd.h
+ABI_VERSION = 4  # PKD_ABI_VERSION of include/pkd.h
 
 # every symbol include/pkd.h declares
 EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
@@ -39,7 +39,7 @@ EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
             "pkd_run_merge", "pkd_merge_states", "pkd_check_status",
             "pkd_run_static", "pkd_prefix_workspace_size", "pkd_plan_shared_prefix",
             "pkd_run_shared_prefix", "pkd_append_kv", "pkd_run_shared_prefix_states",
-            "pkd_run_cascade", "pkd_run_cascade_merge")
+            "pkd_run_cascade", "pkd_run_cascade_merge", "pkd_run_decode_states")
 
 
 class PkdError(RuntimeError):
@@ -104,6 +104,8 @@ def load():
     lib.pkd_run.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, vp, vp, vp,
                             ctypes.c_size_t, ctypes.c_float, vp, vp, vp]
     lib.pkd_run_decode.argtypes = lib.pkd_run.argtypes
+    lib.pkd_run_decode_states.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, vp, vp,
+                                          vp, ctypes.c_size_t, ctypes.c_float, vp]
     lib.pkd_run_merge.argtypes = [ctypes.POINTER(Plan), vp, vp, ctypes.c_size_t,
                                   vp, vp, vp]
     lib.pkd_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int64,
@@ -247,10 +249,25 @@ def run(plan_: Plan, q, k_pages, v_pages, kv_indptr, kv_indices, kv_last_page_le
     """Decode attention for a planned batch; returns (out, lse).
 
     ``phase`` selects the C entry point: "both" (pkd_run), "decode"
-    (pkd_run_decode) or "merge" (pkd_run_merge; out and lse must be given).
+    (pkd_run_decode), "merge" (pkd_run_merge; out and lse must be given) or
+    "decode_states" (pkd_run_decode_states: every request's state stays fp32
+    in ``float_ws``; returns None).
     """
     import torch
     p = plan_.problem
+    if phase == "decode_states":
+        for t in (q, k_pages, v_pages):
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+        if _dtype_code(q.dtype) != p.dtype or k_pages.dtype != q.dtype or \
+                v_pages.dtype != q.dtype:
+            raise ValueError("dtype does not match the plan")
+        _check(load().pkd_run_decode_states(
+            ctypes.byref(plan_), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_indptr),
+            _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(int_ws), _ptr(float_ws),
+            float_ws.numel() * float_ws.element_size(), float(sm_scale),
+            _stream_ptr(stream)))
+        return None
     if out is None:
         out = torch.empty((p.batch, p.num_qo_heads, p.head_dim), dtype=q.dtype,
                           device=q.device)
@@ -448,7 +465,8 @@ def run_cascade(plan_: Plan, prefix_plan: PrefixPlan, q, k_pages, v_pages, kv_in
 def run_cascade_merge(plan_: Plan, prefix_plan: PrefixPlan, ws, prefix_ws, out, lse,
                       stream=None):
     """The last launch of :func:`run_cascade`: folds the prefix chunk states
-    into the suffix states in (out, lse)."""
+    and the fp32 suffix states that ``ws.run(..., phase="decode_states")``
+    left in ``ws`` into (out, lse)."""
     fbytes = ws.float_ws.numel() * ws.float_ws.element_size()
     pbytes = prefix_ws.float_ws.numel() * prefix_ws.float_ws.element_size()
     _check(load().pkd_run_cascade_merge(

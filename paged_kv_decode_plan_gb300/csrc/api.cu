@@ -122,32 +122,45 @@ pkd_status check_cascade(const pkd_plan_t *plan, const pkd_prefix_plan_t *prefix
   return PKD_OK;
 }
 
-// Checks a decode launch and starts the decode kernel (pkd_run_decode; the
-// cascade launches it as a programmatic dependent of the prefix kernel).
+// fp32 state slots of a states-only decode: the plan's partial slots, then
+// one per request (pkd_run_decode_states).
+size_t states_bytes(const pkd_plan_t &plan) {
+  const pkd_problem &p = plan.problem;
+  return static_cast<size_t>(plan.num_partials + p.batch) *
+         static_cast<size_t>(pkd::partial_slot_floats(p.num_qo_heads, p.head_dim)) *
+         sizeof(float);
+}
+
+// Checks a decode launch and starts the decode kernel (pkd_run_decode, or
+// pkd_run_decode_states with states_only; the cascade launches the latter as
+// a programmatic dependent of the prefix kernel).
 pkd_status launch_decode_checked(const pkd_plan_t *plan, const void *q, const void *k_pages,
                                  const void *v_pages, const int32_t *kv_indptr_d,
                                  const int32_t *kv_indices_d,
                                  const int32_t *kv_last_page_len_d, void *int_ws_dev,
                                  void *float_ws_dev, size_t float_ws_bytes, float sm_scale,
-                                 void *out, float *lse, void *stream, int programmatic) {
+                                 void *out, float *lse, void *stream, int programmatic,
+                                 int states_only, bool check_only = false) {
   if (!plan || !plan->valid) return fail(PKD_ERR_INVALID_ARG, "plan not valid");
   const pkd_problem &p = plan->problem;
   pkd_status st = pkd::check_problem(p, true);
   if (st != PKD_OK) return st;
   if (p.batch == 0) return PKD_OK;
-  if (!q || !out || !lse || !kv_indptr_d || !kv_last_page_len_d || !int_ws_dev)
+  if (!q || (!states_only && (!out || !lse)) || !kv_indptr_d || !kv_last_page_len_d ||
+      !int_ws_dev)
     return fail(PKD_ERR_INVALID_ARG, "null device pointer");
   if (plan->total_tokens > 0 && (!k_pages || !v_pages || !kv_indices_d))
     return fail(PKD_ERR_INVALID_ARG, "null page pool or page ids");
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) ||
       !aligned16(out) || !aligned16(int_ws_dev) || !aligned16(float_ws_dev))
     return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
-  if (plan->num_partials > 0 &&
-      (!float_ws_dev ||
-       float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed)))
+  const size_t need =
+      states_only ? states_bytes(*plan) : static_cast<size_t>(plan->float_ws_bytes_needed);
+  if ((plan->num_partials > 0 || states_only) && (!float_ws_dev || float_ws_bytes < need))
     return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the plan needs");
   if (!std::isfinite(sm_scale) || !(sm_scale > 0.f))
     return fail(PKD_ERR_INVALID_ARG, "sm_scale must be finite and positive");
+  if (check_only) return PKD_OK;
 
   pkd::DecodeArgs a;
   a.q = q;
@@ -174,6 +187,7 @@ pkd_status launch_decode_checked(const pkd_plan_t *plan, const void *q, const vo
   a.loader = p.kv_loader;
   a.layout = p.kv_layout;
   a.programmatic = programmatic;
+  a.states_only = states_only;
   cudaError_t e = static_cast<cudaError_t>(pkd::launch_decode(a, stream));
   if (e == cudaErrorNotSupported)
     return fail(PKD_ERR_UNSUPPORTED, "TMA tensor maps unavailable for these pages");
@@ -249,7 +263,19 @@ pkd_status pkd_run_decode(const pkd_plan_t *plan, const void *q,
   pkd::clear_error();
   return launch_decode_checked(plan, q, k_pages, v_pages, kv_indptr_d, kv_indices_d,
                                kv_last_page_len_d, int_ws_dev, float_ws_dev, float_ws_bytes,
-                               sm_scale, out, lse, stream, 0);
+                               sm_scale, out, lse, stream, 0, 0);
+}
+
+pkd_status pkd_run_decode_states(const pkd_plan_t *plan, const void *q,
+                                 const void *k_pages, const void *v_pages,
+                                 const int32_t *kv_indptr_d, const int32_t *kv_indices_d,
+                                 const int32_t *kv_last_page_len_d, void *int_ws_dev,
+                                 void *float_ws_dev, size_t float_ws_bytes, float sm_scale,
+                                 void *stream) {
+  pkd::clear_error();
+  return launch_decode_checked(plan, q, k_pages, v_pages, kv_indptr_d, kv_indices_d,
+                               kv_last_page_len_d, int_ws_dev, float_ws_dev, float_ws_bytes,
+                               sm_scale, nullptr, nullptr, stream, 0, 1);
 }
 
 pkd_status pkd_run_merge(const pkd_plan_t *plan, const void *int_ws_dev,
@@ -466,9 +492,8 @@ pkd_status pkd_run_cascade_merge(const pkd_plan_t *plan, void *int_ws_dev,
   if (prefix_float_ws_bytes < static_cast<size_t>(prefix_plan->float_ws_bytes_needed))
     return fail(PKD_ERR_WORKSPACE, "prefix float workspace smaller than its plan needs");
   const bool capture = capturing(stream);
-  if ((plan->num_partials > 0 || capture) &&
-      (!float_ws_dev || float_ws_bytes < static_cast<size_t>(plan->float_ws_bytes_needed)))
-    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the plan needs");
+  if (!float_ws_dev || float_ws_bytes < states_bytes(*plan))
+    return fail(PKD_ERR_WORKSPACE, "float workspace smaller than the suffix states need");
   const Bounds bounds = launch_bounds(*plan, float_ws_bytes, capture);
   pkd::CascadeMergeArgs m;
   m.image = static_cast<const int32_t *>(int_ws_dev);
@@ -504,16 +529,24 @@ pkd_status pkd_run_cascade(const pkd_plan_t *plan, const void *q, const void *k_
   if (plan->problem.batch == 0) return PKD_OK;
   if (!out || !lse || !prefix_float_ws_dev)
     return fail(PKD_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned16(out))
+    return fail(PKD_ERR_UNSUPPORTED, "device pointers must be 16-byte aligned");
   if (prefix_float_ws_bytes < static_cast<size_t>(prefix_plan->float_ws_bytes_needed))
     return fail(PKD_ERR_WORKSPACE, "prefix float workspace smaller than its plan needs");
+  st = launch_decode_checked(plan, q, k_pages, v_pages, kv_indptr_d, kv_indices_d,
+                             kv_last_page_len_d, int_ws_dev, float_ws_dev, float_ws_bytes,
+                             sm_scale, nullptr, nullptr, stream, 1, 1, true);
+  if (st != PKD_OK) return st;
   st = start_prefix(prefix_plan, q, k_pages, v_pages, prefix_int_ws_dev,
                     prefix_float_ws_dev, prefix_float_ws_bytes, sm_scale, stream);
   if (st != PKD_OK) return st;
   // the suffix decode reads nothing the prefix kernel writes: it may start as
-  // the prefix kernel's CTAs retire (and waits for that grid before exiting)
+  // the prefix kernel's CTAs retire (and waits for that grid before exiting).
+  // It leaves every request's suffix state in fp32, so the final state is
+  // rounded to the output type once.
   st = launch_decode_checked(plan, q, k_pages, v_pages, kv_indptr_d, kv_indices_d,
                              kv_last_page_len_d, int_ws_dev, float_ws_dev, float_ws_bytes,
-                             sm_scale, out, lse, stream, 1);
+                             sm_scale, nullptr, nullptr, stream, 1, 1);
   if (st != PKD_OK) return st;
   return pkd_run_cascade_merge(plan, int_ws_dev, float_ws_dev, float_ws_bytes, prefix_plan,
                                prefix_int_ws_dev, prefix_float_ws_dev,

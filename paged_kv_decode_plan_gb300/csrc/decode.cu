@@ -99,6 +99,8 @@ struct Params {
   int grid;           // CTAs launched
   int hnd;            // page tensors are HND
   int programmatic;   // launched as a programmatic dependent (host side only)
+  int states_only;    // every request's state as fp32: unsplit request b in
+                      // slot num_partials + b, nothing into out / lse
   // batch: requests the q / out / lse / page-table buffers hold; a plan may
   // cover fewer (a captured launch replayed with a later, smaller plan)
 };
@@ -127,6 +129,8 @@ __device__ Unit read_unit(const Params &p, const int32_t *units, int u,
     r.t0 = r.t1 = 0;
     return r;
   }
+  // the kernel checked num_partials + batch <= max_partials for this mode
+  if (p.states_only && r.slot < 0) r.slot = num_partials + r.req;
   const int pb = ptx::ldg_keep(p.indptr + r.req, keep);
   const int pe = ptx::ldg_keep(p.indptr + r.req + 1, keep);
   long long len = 0;
@@ -570,6 +574,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
       hdr[kHNumQoHeads] != p.hq || hdr[kHPageSize] != p.page_size ||
       num_ctas != p.grid || num_units < 0 || num_partials < 0 ||
       num_partials > p.max_partials || hdr[kHNumSplit] < 0 ||
+      (p.states_only && num_partials + hdr[kHBatch] > p.max_partials) ||
       image_offsets(num_ctas, num_units, hdr[kHNumSplit]).end > p.image_words) {
     if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
     ptx::wait_primary_grid();
@@ -824,6 +829,7 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   prm.grid = a.num_ctas;
   prm.hnd = a.layout == PKD_LAYOUT_HND;
   prm.programmatic = a.programmatic;
+  prm.states_only = a.states_only;
 
   CUtensorMap mk;
   CUtensorMap mv;

@@ -109,11 +109,12 @@ __global__ void __launch_bounds__(kMergeThreads)
 // states": the states of the shared prefix and of a request's own suffix
 // merge into the state over both).  One warp per (request b, query head h)
 // row folds the prefix's chunk states (slots b * chunks .. b * chunks +
-// chunks - 1 of the prefix workspace) and the suffix state: the request's
-// partial slots if the suffix plan split it, else the (out, lse) row the
-// decode kernel wrote, which is read before the final state overwrites it.
-// The suffix plan lists its split requests in increasing order; a warp finds
-// b among them 32 at a time with a ballot.
+// chunks - 1 of the prefix workspace) and the suffix state, fp32 throughout
+// (the decode kernel ran in its states-only mode): the request's partial
+// slots if the suffix plan split it, else slot num_partials + b.  The final
+// state is rounded to the output type once.  The suffix plan lists its split
+// requests in increasing order; a warp finds b among them 32 at a time with a
+// ballot.
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads)
     cascade_merge_kernel(const int32_t *image, const float *partials,
@@ -129,7 +130,8 @@ __global__ void __launch_bounds__(kMergeThreads)
   // both images must be the plans the host made for this launch
   if (image[kHMagic] != kMagic || image[kHBatch] != batch || image[kHNumQoHeads] != hq ||
       num_ctas < 0 || num_units < 0 || num_split < 0 || num_partials < 0 ||
-      num_partials > max_partials || o.end > image_words ||
+      num_partials > max_partials || num_partials + batch > max_partials ||
+      o.end > image_words ||
       prefix_image[kHMagic] != kPrefixMagic || prefix_image[kPBatch] != batch ||
       prefix_image[kPNumQoHeads] != hq || prefix_image[kPChunks] != chunks) {
     if (blockIdx.x == 0 && threadIdx.x == 0)
@@ -141,8 +143,8 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int32_t *merge_req = image + o.merge_req;
   const long long slot_floats = partial_slot_floats(hq, kHeadDim);
   const long long rows = static_cast<long long>(batch) * hq;
-  // a programmatic dependent of the decode kernel, which started after the
-  // prefix kernel had finished: once the decode kernel is complete, both
+  // a programmatic dependent of the decode kernel, whose threads wait for the
+  // prefix kernel before exiting: once the decode kernel is complete, both
   // kernels' states are in place
   ptx::wait_primary_grid();
   for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -167,11 +169,9 @@ __global__ void __launch_bounds__(kMergeThreads)
       const int s1 = min(num_partials, merge_indptr[split + 1]);
       fold_states(partials, slot_floats, hq, h, s0, s1, 1, lane, m, ws, acc);
     } else {
-      const uint2 raw = reinterpret_cast<const uint2 *>(out + row * kHeadDim)[lane];
-      const float2 v01 = ptx::unpack2<T>(raw.x), v23 = ptx::unpack2<T>(raw.y);
-      fold_one(lse[row], make_float4(v01.x, v01.y, v23.x, v23.y), m, ws, acc);
+      fold_states(partials, slot_floats, hq, h, num_partials + b, num_partials + b + 1, 1,
+                  lane, m, ws, acc);
     }
-    __syncwarp();  // every lane has read the row before it is overwritten
     write_state<T>(out, lse, b, hq, h, lane, m, ws, acc);
   }
 }

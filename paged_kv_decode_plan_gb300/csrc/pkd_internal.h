@@ -96,6 +96,7 @@ struct DecodeArgs {
   int loader;  // pkd_loader of the problem
   int layout;  // pkd_layout of the page tensors
   int programmatic;  // launch as a programmatic dependent of the previous kernel
+  int states_only;   // fp32 states for every request (slot num_partials + b when unsplit)
 };
 int launch_decode(const DecodeArgs &a, void *stream);
 

@@ -88,8 +88,11 @@ void workspace_bytes(const pkd_problem &p, size_t *int_ws, size_t *float_ws,
   const size_t int_bytes = static_cast<size_t>(o.end) * sizeof(int32_t);
   if (int_ws) *int_ws = int_bytes;
   if (staging) *staging = int_bytes;
+  // partial slots for every unit, plus one per request: a states-only decode
+  // (the cascade's suffix) puts unsplit request b's state in slot
+  // num_partials + b
   if (float_ws)
-    *float_ws = static_cast<size_t>(units) *
+    *float_ws = static_cast<size_t>(units + cap_batch) *
                 partial_slot_floats(p.num_qo_heads, p.head_dim) * sizeof(float);
 }
 

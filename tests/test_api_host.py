@@ -1,7 +1,7 @@
 """Host-side argument checks of the cascade entry points (no GPU needed).
 
-pkd_run_cascade, pkd_run_cascade_merge and pkd_run_shared_prefix_states
-check plans, problem agreement, pointers and workspace sizes on the host and
+pkd_run_cascade, pkd_run_cascade_merge, pkd_run_shared_prefix_states and
+pkd_run_decode_states check plans, problem agreement, pointers and workspace sizes on the host and
 return a status before any CUDA call; these tests pass placeholder device
 addresses that a launch would need, so a check that let them through would
 fail here loudly rather than touch memory.
@@ -42,11 +42,18 @@ def _prefix_plan(suffix, **override):
     return pp
 
 
-def _cascade(plan, pp, out=FAKE, lse=FAKE, prefix_float=FAKE, prefix_bytes=1 << 30):
+def _cascade(plan, pp, out=FAKE, lse=FAKE, prefix_float=FAKE, prefix_bytes=1 << 30,
+             float_bytes=1 << 30):
     lib = pkd.load()
     return lib.pkd_run_cascade(ctypes.byref(plan), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
-                               FAKE, 1 << 30, ctypes.byref(pp), FAKE, prefix_float,
+                               FAKE, float_bytes, ctypes.byref(pp), FAKE, prefix_float,
                                prefix_bytes, ctypes.c_float(0.088), out, lse, None)
+
+
+def _states_bytes(plan):
+    """fp32 slots a states-only decode needs: the plan's partial slots plus
+    one per request."""
+    return (plan.num_partials + plan.problem.batch) * 4 * (32 * 128 + 32)
 
 
 def _message():
@@ -107,3 +114,29 @@ def test_prefix_states_check_the_plan_and_pointers():
                                             None) == INVALID_ARG
     assert lib.pkd_run_shared_prefix_states(ctypes.byref(pp), FAKE, FAKE, FAKE, FAKE, FAKE,
                                             8, ctypes.c_float(0.088), None) == WORKSPACE
+
+
+def test_states_only_decode_checks_its_float_workspace():
+    plan = _suffix_plan()
+    lib = pkd.load()
+    need = _states_bytes(plan)
+    assert need > plan.float_ws_bytes_needed   # one slot per request on top
+
+    def run(float_ws, nbytes):
+        return lib.pkd_run_decode_states(ctypes.byref(plan), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                         FAKE, FAKE, float_ws, nbytes, ctypes.c_float(0.088),
+                                         None)
+    assert run(FAKE, need - 1) == WORKSPACE
+    assert run(None, need) == WORKSPACE
+    assert "float workspace" in _message()
+
+
+def test_cascade_checks_the_suffix_states_workspace():
+    plan = _suffix_plan()
+    pp = _prefix_plan(plan)
+    assert _cascade(plan, pp, float_bytes=_states_bytes(plan) - 1) == WORKSPACE
+    assert "float workspace" in _message()
+    lib = pkd.load()
+    assert lib.pkd_run_cascade_merge(ctypes.byref(plan), FAKE, FAKE, _states_bytes(plan) - 1,
+                                     ctypes.byref(pp), FAKE, FAKE, 1 << 30, FAKE, FAKE,
+                                     None) == WORKSPACE

@@ -94,8 +94,9 @@ def test_cascade_pieces_equal_the_single_call():
     one, one_lse = pkd.run_cascade(plan, pplan, dev.q, dev.k, dev.v, indptr, indices, last,
                                    ws, pws, wl.sm_scale)
     pws.run_states(pplan, dev.q, dev.k, dev.v, wl.sm_scale)
-    out, lse = ws.run(plan, dev.q, dev.k, dev.v, indptr, indices, last, wl.sm_scale,
-                      phase="decode")
+    ws.run(plan, dev.q, dev.k, dev.v, indptr, indices, last, wl.sm_scale,
+           phase="decode_states")
+    out, lse = torch.empty_like(one), torch.empty_like(one_lse)
     pkd.run_cascade_merge(plan, pplan, ws, pws, out, lse)
     torch.cuda.synchronize()
     assert torch.equal(out, one) and torch.equal(lse, one_lse)
@@ -208,3 +209,37 @@ def test_cascade_hnd_pages_equal_nhd(dtype):
     assert torch.equal(results[0][0], results[1][0])
     assert torch.equal(results[0][1], results[1][1])
     gh.compare(results[1][0], results[1][1], *_reference(wl, prefix, suffix), dtype)
+
+
+def _random_case(i):
+    """Seeded draw: batch, heads (any group up to 16, so the prefix kernel's
+    plain query loads for 128 % g != 0 are covered), page size, prefix and
+    suffix lengths (empty ones included), dtype, CTA budget, chunks."""
+    rng = np.random.default_rng([4241, i])
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    group = int(rng.choice([1, 2, 3, 4, 5, 6, 8, 12, 16]))
+    batch = int(rng.integers(1, 41))
+    prefix_len = int(rng.choice([0, 1, int(rng.integers(2, 200)), int(rng.integers(200, 4000))]))
+    suffix = rng.integers(0, 2000, batch)
+    suffix[rng.random(batch) < 0.15] = 0
+    return dict(batch=batch, hq=hkv * group, hkv=hkv, page=int(rng.choice([16, 32, 64])),
+                prefix_len=prefix_len, suffix=[int(x) for x in suffix],
+                dtype="f16" if rng.random() < 0.5 else "bf16",
+                num_ctas=int(rng.choice([0, 5, 37, 152])),
+                min_chunks=int(rng.choice([1, 2, 4])), seed=300 + i)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_cascade_random_cases(i):
+    c = _random_case(i)
+    wl, pre_pages, pre_last, prefix, suffix = _case(c["batch"], c["hq"], c["hkv"], c["page"],
+                                                    c["prefix_len"], c["suffix"], c["dtype"],
+                                                    c["seed"])
+    dev = gh.DeviceBatch(wl)
+    ws, plan, pws, pplan = _setup(wl, pre_pages, pre_last, suffix, c["num_ctas"],
+                                  c["min_chunks"])
+    out, lse = pkd.run_cascade(plan, pplan, dev.q, dev.k, dev.v, *gh.device_table(suffix),
+                               ws, pws, wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pkd.check_status(ws.int_ws) == 0 and pkd.check_status(pws.int_ws) == 0
+    gh.compare(out, lse, *_reference(wl, prefix, suffix), c["dtype"])

@@ -120,3 +120,6 @@ def test_capacity_bound_holds_for_extreme_splits():
         ib, fb, sb = pkd.workspace_size(prob)
         assert plan.int_ws_bytes_used <= ib and sb == ib
         assert plan.float_ws_bytes_needed <= fb
+        # a states-only decode also keeps one fp32 state per unsplit request
+        slot = 4 * (32 * 128 + 32)
+        assert (plan.num_partials + len(lengths)) * slot <= fb
