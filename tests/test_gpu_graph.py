@@ -162,3 +162,77 @@ def test_zero_requests():
                               base.k_pages, base.v_pages, full, base.sm_scale)
     ref_out, ref_lse = gh.oracle_ref(wl)
     gh.compare(out[: full.batch], lse[: full.batch], ref_out, ref_lse, dtype)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_replays(seed):
+    """One capture at a random capacity (max batch, CTAs, minimum chunks, page
+    size, heads, dtype), replayed for five later plans of random batch and
+    lengths (all-empty and tiny batches included); every replay against the
+    oracle."""
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device")
+    rng = np.random.default_rng([5003, seed])
+    max_batch = int(rng.integers(1, 13))
+    page = int(rng.choice([1, 3, 16, 64]))
+    hkv = int(rng.choice([1, 2, 8]))
+    hq = hkv * int(rng.choice([1, 4, 5, 8]))
+    dtype = "f16" if seed % 2 == 0 else "bf16"
+    ctas = int(rng.choice([3, 40, 152]))
+    m = int(rng.choice([1, 3]))
+    max_len = 2500
+    pool = max_batch * ((max_len + page - 1) // page) + 8
+    base = workloads.make_paged("replay", [1] * max_batch, num_qo_heads=hq, num_kv_heads=hkv,
+                                page_size=page, dtype=dtype, seed=seed + 50, pool_pages=pool)
+    dev = gh.DeviceBatch(base)
+    prob = pkd.make_problem(batch=max_batch, num_qo_heads=hq, num_kv_heads=hkv,
+                            page_size=page, dtype=dtype, num_pages=pool, num_ctas=ctas,
+                            min_chunks_per_request=m, max_batch=max_batch)
+    ws = pkd.Workspace(prob)
+    indptr_d = torch.zeros(max_batch + 1, dtype=torch.int32, device="cuda")
+    indices_d = torch.zeros(pool, dtype=torch.int32, device="cuda")
+    last_d = torch.zeros(max_batch, dtype=torch.int32, device="cuda")
+    out = torch.zeros_like(dev.q)
+    lse = torch.zeros(dev.q.shape[:2], dtype=torch.float32, device="cuda")
+
+    def table(lengths):
+        perm = rng.permutation(pool)
+        return workloads.table_from_lengths(lengths, page, perm)
+
+    def load_table(t):
+        indptr_d.zero_()
+        last_d.zero_()
+        indptr_d[: t.batch + 1].copy_(torch.from_numpy(t.kv_indptr))
+        if t.kv_indices.size:
+            indices_d[: t.kv_indices.size].copy_(torch.from_numpy(t.kv_indices))
+        if t.batch:
+            last_d[: t.batch].copy_(torch.from_numpy(t.kv_last_page_len))
+
+    first = table([int(x) for x in rng.integers(1, max_len, max_batch)])
+    load_table(first)
+    plan = ws.plan(first.kv_indptr, first.kv_last_page_len, first.kv_indices)
+    ws.run(plan, dev.q, dev.k, dev.v, indptr_d, indices_d, last_d, base.sm_scale,
+           out=out, lse=lse)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ws.run(plan, dev.q, dev.k, dev.v, indptr_d, indices_d, last_d, base.sm_scale,
+               out=out, lse=lse)
+
+    later = [[int(x) for x in rng.integers(0, max_len, int(rng.integers(1, max_batch + 1)))]
+             for _ in range(3)]
+    later += [[0] * int(rng.integers(1, max_batch + 1)),                 # all empty
+              [int(x) for x in rng.integers(1, 4, max_batch)]]          # tiny
+    for lengths in later:
+        t = table(lengths)
+        load_table(t)
+        ws.plan(t.kv_indptr, t.kv_last_page_len, t.kv_indices, batch=t.batch)
+        out.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pkd.check_status(ws.int_ws) == 0, lengths
+        wl = workloads.PagedBatch("replay", hq, hkv, 128, dtype, base.q[: t.batch],
+                                  base.k_pages, base.v_pages, t, base.sm_scale)
+        ref_out, ref_lse = gh.oracle_ref(wl)
+        gh.compare(out[: t.batch], lse[: t.batch], ref_out, ref_lse, dtype)
