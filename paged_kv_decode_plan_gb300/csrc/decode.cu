@@ -5,13 +5,16 @@
 // tokens of every key/value head (16 * Hkv * 512 bytes of K and V).
 //
 // Roles inside a CTA:
-//  * one loader warp fills a ring of shared-memory stages.  By default it
-//    issues one 1-D bulk copy (cp.async.bulk) per (tensor, token): in NHD
-//    memory a token's rows of all heads are contiguous, so this works for
-//    any page size.  On request (PKD_LOADER_TMA_TILES), when pages hold
-//    whole 16-token tiles, it issues TMA tiled loads (cp.async.bulk.tensor,
-//    128-byte swizzle), one 16 x 64-element box per (tensor, head, d-half).
-//    Copies complete on the stage's "full" mbarrier.
+//  * one loader warp fills a ring of shared-memory stages.  For NHD pages it
+//    issues by default one 1-D bulk copy (cp.async.bulk) per (tensor, token):
+//    a token's rows of all heads are contiguous there, so this works for any
+//    page size.  When pages hold whole 16-token tiles it can instead issue
+//    TMA tiled loads (cp.async.bulk.tensor, 128-byte swizzle), one box per
+//    (tensor, head, d-half): the default for HND pages ([page][head][token]
+//    [d]), where bulk copies would be one per (tensor, token, head).  Copies
+//    complete on the stage's "full" mbarrier.  K/V copies carry an
+//    evict-first L2 policy (read once); the plan, page table and queries are
+//    loaded, and outputs and partial states stored, with an evict-last one.
 //  * eight consumer warps compute.  Warp w owns key/value head
 //    w / (8 / Hkv) and a slice of that head's query group, so no two warps
 //    share an output row.  With the query group as the N = 8 side of
@@ -25,8 +28,11 @@
 //        through movmatrix.  For bfloat16, P is split into hi + lo parts
 //        (8 significant bits each) and multiplied twice; row sums are taken
 //        over exactly the values multiplied.
-// Every mbarrier wait is bounded; a wait that runs out records
-// PKD_DEVICE_TIMEOUT in the status word and the CTA stops.
+// A unit's result goes to out / lse when its request is not split, else to
+// its fp32 partial slot; in the states-only mode (the cascade's suffix) an
+// unsplit request b also goes to an fp32 slot, num_partials + b.  Every
+// mbarrier wait is bounded; a wait that runs out records PKD_DEVICE_TIMEOUT
+// in the status word and the CTA stops.
 //
 // Sources (page title, section):
 //  - "FlashInfer" (aiwiki.ai/wiki/flashinfer), "Block-sparse cache
