@@ -7,7 +7,9 @@ kernels.  PyTorch supplies device memory and streams.  If the library is
 missing, every call raises; there is no other implementation to fall back to.
 
 Entry points (same names as the C ABI without the ``pkd_`` prefix):
-``workspace_size``, ``plan_host``, ``plan``, ``run``, ``merge_states``,
+``workspace_size``, ``plan_host``, ``plan``, ``run`` (its ``phase`` picks
+``pkd_run``, ``pkd_run_decode``, ``pkd_run_merge`` or
+``pkd_run_decode_states``), ``run_static``, ``merge_states``,
 ``check_status``, the shared-prefix calls (``plan_shared_prefix``,
 ``run_shared_prefix``, ``run_shared_prefix_states``, ``run_cascade``,
 ``run_cascade_merge``), ``append_kv``, plus :class:`Workspace` and
