@@ -283,3 +283,51 @@ def test_run_rejects_bad_arguments():
         pkd.run(plan, dev.q, dev.k, dev.v, indptr, indices, last, ws.int_ws,
                 ws.float_ws[:16], wl.sm_scale)
     assert e.value.status == -3
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_decode_states_hold_every_request_in_fp32(dtype):
+    """pkd_run_decode_states: split requests' partial states in their plan
+    slots (folded here by the oracle's merge), every other request's state in
+    slot num_partials + b; each request's fp32 state against the oracle, the
+    empty request exactly (0, -inf) ("FlashInfer" (aiwiki.ai/wiki/flashinfer),
+    "Attention states")."""
+    from tests.test_plan_ref import decode_image
+    lengths = [0, 1, 700, 33, 2500, 16, 4000, 130]
+    hq = 32
+    wl = workloads.make_paged("states", lengths, num_qo_heads=hq, num_kv_heads=8,
+                              page_size=16, dtype=dtype, seed=11)
+    dev = gh.DeviceBatch(wl)
+    prob = pkd.make_problem(batch=wl.batch, num_qo_heads=hq, num_kv_heads=8, page_size=16,
+                            dtype=dtype, num_pages=wl.num_pages, num_ctas=20)
+    ws = pkd.Workspace(prob)
+    t = wl.table
+    plan = ws.plan(t.kv_indptr, t.kv_last_page_len, t.kv_indices)
+    assert 0 < plan.num_split_requests < wl.batch
+    ws.run(plan, dev.q, dev.k, dev.v, *gh.device_table(t), wl.sm_scale,
+           phase="decode_states")
+    torch.cuda.synchronize()
+    assert pkd.check_status(ws.int_ws) == 0
+    slot_floats = hq * 128 + (hq + 3) // 4 * 4
+    nslots = plan.num_partials + wl.batch
+    f = ws.float_ws[: nslots * slot_floats * 4].view(torch.float32).cpu().numpy()
+    f = f.reshape(nslots, slot_floats).astype(np.float64)
+    o, s = f[:, : hq * 128].reshape(nslots, hq, 128), f[:, hq * 128: hq * 128 + hq]
+    _, image = pkd.plan_host(prob, t.kv_indptr, t.kv_last_page_len)
+    _, _, _, merge_indptr, merge_req = decode_image(image)
+    ref_out, ref_lse = gh.oracle_ref(wl)
+    ref_out, ref_lse = ref_out.reshape(wl.batch, hq, 128), ref_lse.reshape(wl.batch, hq)
+    for b in range(wl.batch):
+        if b in merge_req:
+            i = merge_req.index(b)
+            slots = range(merge_indptr[i], merge_indptr[i + 1])
+            v, lse = o[slots[0]], s[slots[0]]
+            for j in slots[1:]:
+                v, lse = oracle.merge(v, lse, o[j], s[j])
+        else:
+            v, lse = o[plan.num_partials + b], s[plan.num_partials + b]
+        if lengths[b] == 0:
+            assert np.all(v == 0.0) and np.all(lse == -np.inf), b
+            continue
+        assert np.abs(v - ref_out[b]).max() <= gh.OUT_TOL, b
+        assert np.abs(lse - ref_lse[b]).max() <= gh.LSE_TOL, b
