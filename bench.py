@@ -756,7 +756,7 @@ def cpu_baseline(wl, budget_s: float, kind="oracle"):
     done_req = 0
     elapsed = 0.0
     b = 0
-    while elapsed < budget_s and done_req < 4 * wl.batch:
+    while elapsed < budget_s and done_req < 64 * wl.batch:
         rows = _oracle_rows_for(wl, b, 1)
         t0 = time.perf_counter()
         oracle.decode(*codes, t.kv_indptr, t.kv_indices, t.kv_last_page_len,
