@@ -486,13 +486,7 @@ class Runner:
 
     def kv_bytes(self):
         """Algorithmic KV bytes per step (a shared prefix counted once)."""
-        wl = self.wl
-        per_token = 2 * wl.num_kv_heads * wl.head_dim * wl.k_pages.element_size()
-        if wl.name == "cascade":
-            prefix = wl.extra_tables["prefix"]
-            prefix_tokens = int(prefix.lengths()[0]) if prefix.batch else 0
-            return (prefix_tokens + int(wl.extra_tables["suffix"].lengths().sum())) * per_token
-        return int(wl.table.lengths().sum()) * per_token
+        return workload_kv_bytes(self.wl)
 
     def total_bytes(self):
         """All algorithmic bytes a step moves: KV (shared prefix once), the
@@ -544,6 +538,29 @@ def _layout(sizes, align=256):
         offs.append(off)
         off += (n + align - 1) // align * align
     return offs, off
+
+
+def workload_kv_bytes(wl):
+    """Algorithmic KV bytes of one pass over a workload (a shared prefix
+    counted once)."""
+    per_token = 2 * wl.num_kv_heads * wl.head_dim * wl.k_pages.element_size()
+    if wl.name == "cascade":
+        prefix = wl.extra_tables["prefix"]
+        prefix_tokens = int(prefix.lengths()[0]) if prefix.batch else 0
+        return (prefix_tokens + int(wl.extra_tables["suffix"].lengths().sum())) * per_token
+    return int(wl.table.lengths().sum()) * per_token
+
+
+def workload_config(wl):
+    """The JSON line's config: the workload, its sizes and the L2 note."""
+    kv = workload_kv_bytes(wl)
+    return {"workload": DESCRIPTIONS[wl.name], "name": wl.name,
+            "batch": wl.batch, "num_qo_heads": wl.num_qo_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+            "page_size": wl.page_size, "kv_bytes_per_step": kv,
+            "l2": ("inputs larger than L2 (KV %.0f MB vs 129 MB), no flush" % (kv / 1e6))
+            if kv > 2 * L2_BYTES else "KV fits in L2: warm-L2 number",
+            "parallelism": "replicas (weak scaling, no collective)"}
 
 
 def pack_table(t):
@@ -637,14 +654,7 @@ def run_ours(args, ranks):
         "ms_per_step": round(agg["ms_per_step"], 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "accumulate": "f32",
         "data": "synthetic (seeded N(0,1), shapes of the workload)",
-        "config": {"workload": DESCRIPTIONS[wl.name], "name": wl.name,
-                   "batch": wl.batch, "num_qo_heads": wl.num_qo_heads,
-                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
-                   "page_size": wl.page_size, "kv_bytes_per_step": runner.kv_bytes(),
-                   "l2": ("inputs larger than L2 (KV %.0f MB vs 129 MB), no flush"
-                          % (runner.kv_bytes() / 1e6)) if runner.kv_bytes() > 2 * L2_BYTES
-                   else "KV fits in L2: warm-L2 number",
-                   "parallelism": "replicas (weak scaling, no collective)"},
+        "config": workload_config(wl),
         "us_per_batch": round(agg["ms_per_step"] * 1e3, 2),
         "total_bytes_per_step": runner.total_bytes(),
         "total_gbs": round(runner.total_bytes() * ranks.world / (agg["ms_per_step"] * 1e-3)
@@ -819,10 +829,7 @@ def run_reference(args, ranks):
         "ms_per_step": round(elapsed * 1e3 / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1), shapes of the workload)",
-        "config": {"workload": DESCRIPTIONS[wl.name], "name": wl.name,
-                   "batch": wl.batch, "num_qo_heads": hq,
-                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
-                   "page_size": wl.page_size},
+        "config": workload_config(wl),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s",
                          "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": sample},
