@@ -167,7 +167,9 @@ template <int HKV, int L>
 __device__ __forceinline__ uint32_t kv_offset(int h, int r, int c) {
   using G = Geometry<HKV, L>;
   if (G::kPadded) return r * G::kRowStride + h * kRowBytes + (c << 4);
-  return h * G::kHeadBytes + tile_offset(r, c);
+  // TMA stages: [d-half][head][16 rows][128 B], 128-byte swizzle (every head
+  // block starts on a 1024-byte boundary, so the swizzle row is r & 7)
+  return (c >> 3) * (HKV * kHalfBytes) + h * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
 // ----------------------------------------------------------------- loaders
@@ -205,18 +207,24 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
       }
       if (lane == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, G::kStageBytes);
       __syncwarp();
-      if (lane < 4 * HKV) {
+      if (p.hnd) {
+        // HND: a page holds each head's slots contiguously, so one box of
+        // (64 d, 16 slots, every head) per (tensor, d-half) fills that half
+        if (lane < 4) {
+          const int tensor = lane >> 1, half = lane & 1;
+          const uint32_t dst = stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
+                               half * (HKV * kHalfBytes);
+          ptx::tma_load_4d_hint(dst, tensor ? map_v : map_k, half * 64, slot0, 0, page,
+                                full0 + 8 * s, stream);
+        }
+      } else if (lane < 4 * HKV) {
         const int tensor = lane / (2 * HKV);
         const int head = (lane >> 1) % HKV;
         const int half = lane & 1;
         const uint32_t dst = stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
-                             head * G::kHeadBytes + half * kHalfBytes;
-        if (p.hnd)
-          ptx::tma_load_4d_hint(dst, tensor ? map_v : map_k, half * 64, slot0, head, page,
-                                full0 + 8 * s, stream);
-        else
-          ptx::tma_load_3d_hint(dst, tensor ? map_v : map_k, half * 64, head,
-                                page * p.page_size + slot0, full0 + 8 * s, stream);
+                             half * (HKV * kHalfBytes) + head * kHalfBytes;
+        ptx::tma_load_3d_hint(dst, tensor ? map_v : map_k, half * 64, head,
+                              page * p.page_size + slot0, full0 + 8 * s, stream);
       }
       ++it;
     }
@@ -720,11 +728,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// K or V pages with d innermost: NHD as [token row][head][d] (3-D), HND as
-// [page][head][slot][d] (4-D); boxes of 16 token rows x 1 head x 64
-// elements, 128-byte swizzle.
+// K or V pages with d innermost: NHD as [token row][head][d] (3-D), boxes of
+// 16 token rows x 1 head x 64 elements; HND as [page][head][slot][d] (4-D),
+// boxes of 64 elements x 16 slots x box_heads heads.  128-byte swizzle.
 bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
-                  int page_size, int hkv, int layout) {
+                  int page_size, int hkv, int layout, int box_heads) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return false;
   const cuuint64_t row = kRowBytes;
@@ -733,7 +741,7 @@ bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
                           static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(hkv),
                           static_cast<cuuint64_t>(num_pages)};
     cuuint64_t strides[3] = {row, row * page_size, row * page_size * hkv};
-    cuuint32_t box[4] = {64, kTile, 1, 1};
+    cuuint32_t box[4] = {64, kTile, static_cast<cuuint32_t>(box_heads), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -754,11 +762,11 @@ bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
 // Tensor maps of the last page pools seen (encoding is pure host work, but a
 // serving loop passes the same pools on every step).
 bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
-                 long long num_pages, int page_size, int hkv, int layout) {
+                 long long num_pages, int page_size, int hkv, int layout, int box_heads) {
   struct Entry {
     const void *k, *v;
     long long num_pages;
-    int page_size, hkv, layout;
+    int page_size, hkv, layout, box_heads;
     CUtensorMap mk;
     CUtensorMap mv;
   };
@@ -768,14 +776,14 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
   std::lock_guard<std::mutex> lock(mutex);
   for (const Entry &e : cache)
     if (e.k == k && e.v == v && e.num_pages == num_pages && e.page_size == page_size &&
-        e.hkv == hkv && e.layout == layout && e.k) {
+        e.hkv == hkv && e.layout == layout && e.box_heads == box_heads && e.k) {
       *mk = e.mk;
       *mv = e.mv;
       return true;
     }
   Entry &e = cache[next];
-  if (!encode_pages(&e.mk, k, num_pages, page_size, hkv, layout) ||
-      !encode_pages(&e.mv, v, num_pages, page_size, hkv, layout)) {
+  if (!encode_pages(&e.mk, k, num_pages, page_size, hkv, layout, box_heads) ||
+      !encode_pages(&e.mv, v, num_pages, page_size, hkv, layout, box_heads)) {
     e.k = nullptr;
     return false;
   }
@@ -785,6 +793,7 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
   e.page_size = page_size;
   e.hkv = hkv;
   e.layout = layout;
+  e.box_heads = box_heads;
   next = (next + 1) % 8;
   *mk = e.mk;
   *mv = e.mv;
@@ -795,7 +804,8 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
 
 bool page_tensor_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
                       long long num_pages, int page_size, int hkv, int layout) {
-  return cached_maps(mk, mv, k, v, num_pages, page_size, hkv, layout);
+  // the shared-prefix kernel loads one head per box
+  return cached_maps(mk, mv, k, v, num_pages, page_size, hkv, layout, 1);
 }
 
 bool query_tensor_map(CUtensorMap *map, const void *q, int batch, int hq, int group) {
@@ -852,8 +862,11 @@ int launch_decode(const DecodeArgs &a, void *stream) {
       (a.loader == PKD_LOADER_AUTO && a.layout == PKD_LAYOUT_HND && tiles_fit);
   int loader = kLoaderBulk;
   if (want_tma) {
+    // HND boxes cover every head of a page's 16 slots (one box per tensor
+    // and d-half); NHD boxes one head
+    const int box_heads = a.layout == PKD_LAYOUT_HND ? a.num_kv_heads : 1;
     if (!tiles_fit || !cached_maps(&mk, &mv, a.k_pages, a.v_pages, a.num_pages,
-                                   a.page_size, a.num_kv_heads, a.layout))
+                                   a.page_size, a.num_kv_heads, a.layout, box_heads))
       return cudaErrorNotSupported;
     loader = kLoaderTma;
   }
