@@ -70,9 +70,11 @@ typedef enum {
 
 /* How the decode kernel moves K/V pages into shared memory. */
 typedef enum {
-  PKD_LOADER_AUTO = 0,       /* the library's choice: bulk rows for NHD; for HND,
-                                TMA tiles when page_size % 16 == 0, else bulk rows */
-  PKD_LOADER_TMA_TILES = 1,  /* TMA tiled loads of 16-token boxes (page_size % 16 == 0) */
+  PKD_LOADER_AUTO = 0,       /* the library's choice: TMA tiles for HND pages when
+                                page_size % 16 == 0 and for NHD pages of exactly 16
+                                tokens, else bulk rows */
+  PKD_LOADER_TMA_TILES = 1,  /* TMA tiled loads, one box per (tensor, d-half) covering
+                                16 slots of every head (page_size % 16 == 0) */
   PKD_LOADER_BULK_ROWS = 2   /* one bulk copy per token row of all heads (NHD) or per
                                 (token, head) row (HND); any page_size */
 } pkd_loader;

@@ -5,14 +5,16 @@
 // tokens of every key/value head (16 * Hkv * 512 bytes of K and V).
 //
 // Roles inside a CTA:
-//  * one loader warp fills a ring of shared-memory stages.  For NHD pages it
-//    issues by default one 1-D bulk copy (cp.async.bulk) per (tensor, token):
-//    a token's rows of all heads are contiguous there, so this works for any
-//    page size.  When pages hold whole 16-token tiles it can instead issue
-//    TMA tiled loads (cp.async.bulk.tensor, 128-byte swizzle), one box per
-//    (tensor, head, d-half): the default for HND pages ([page][head][token]
-//    [d]), where bulk copies would be one per (tensor, token, head).  Copies
-//    complete on the stage's "full" mbarrier.  K/V copies carry an
+//  * one loader warp fills a ring of shared-memory stages, with one of two
+//    loaders.  Bulk rows: one 1-D bulk copy (cp.async.bulk) per (tensor,
+//    token) for NHD pages, where a token's rows of all heads are contiguous
+//    (any page size), or per (tensor, token, head) for HND pages.  TMA
+//    tiles, when pages hold whole 16-token tiles: both layouts are seen as
+//    [page][head][slot][d] and one box of (64 d, 16 slots, every head) per
+//    (tensor, d-half) fills a stage in four copies (cp.async.bulk.tensor,
+//    128-byte swizzle).  The automatic choice is TMA tiles for HND pages and
+//    NHD pages of 16 tokens, bulk rows otherwise.  Copies complete on the
+//    stage's "full" mbarrier.  K/V copies carry an
 //    evict-first L2 policy (read once); the plan, page table and queries are
 //    loaded, and outputs and partial states stored, with an evict-last one.
 //  * eight consumer warps compute.  Warp w owns key/value head
@@ -184,50 +186,56 @@ __device__ void load_tma(const Params &p, const CUtensorMap *map_k,
   const int lane = threadIdx.x & 31;
   const uint32_t stage0 = ptx::smem_u32(stages);
   const uint64_t stream = ptx::policy_evict_first();  // K/V: read once
-  int it = 0;
-  bool ok = true;
-  for (int u = u_begin; u < u_end && ok; ++u) {
-    const Unit unit = read_unit(p, units, u, num_partials);
-    const int ntiles = unit_tiles(unit);
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = it % kStages;
-      if (!wait_phase(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, abort)) {
-        if (lane == 0) give_up(p, abort);
-        ok = false;
-        break;
-      }
-      const int tok0 = unit.t0 + t * kTile;
-      const int pi = tok0 / p.page_size;
-      const int slot0 = tok0 - pi * p.page_size;
-      int page = ptx::ldg_keep(p.indices + unit.pbase + pi, ptx::policy_evict_last());
-      if (static_cast<unsigned long long>(page) >=
-          static_cast<unsigned long long>(p.num_pages)) {
-        if (lane == 0) flag(p.image, PKD_DEVICE_BAD_PAGE);
-        page = 0;
-      }
-      if (lane == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, G::kStageBytes);
-      __syncwarp();
-      if (p.hnd) {
-        // HND: a page holds each head's slots contiguously, so one box of
-        // (64 d, 16 slots, every head) per (tensor, d-half) fills that half
-        if (lane < 4) {
-          const int tensor = lane >> 1, half = lane & 1;
-          const uint32_t dst = stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
-                               half * (HKV * kHalfBytes);
-          ptx::tma_load_4d_hint(dst, tensor ? map_v : map_k, half * 64, slot0, 0, page,
-                                full0 + 8 * s, stream);
-        }
-      } else if (lane < 4 * HKV) {
-        const int tensor = lane / (2 * HKV);
-        const int head = (lane >> 1) % HKV;
-        const int half = lane & 1;
-        const uint32_t dst = stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
-                             half * (HKV * kHalfBytes) + head * kHalfBytes;
-        ptx::tma_load_3d_hint(dst, tensor ? map_v : map_k, half * 64, head,
-                              page * p.page_size + slot0, full0 + 8 * s, stream);
-      }
-      ++it;
+  const uint64_t keep = ptx::policy_evict_last();     // page ids stay in L2
+  // cursor over the CTA's tiles: (page, slot0) of the next tile, its page id
+  // loaded right after the previous tile's boxes are issued, so that the load
+  // overlaps the wait for a free stage
+  int u = u_begin, t = 0;
+  Unit unit;
+  if (u < u_end) unit = read_unit(p, units, u, num_partials);
+  int page = 0, slot0 = 0;
+  bool have = false;
+  auto describe = [&]() {
+    while (u < u_end && t >= unit_tiles(unit)) {
+      ++u;
+      t = 0;
+      if (u < u_end) unit = read_unit(p, units, u, num_partials);
     }
+    have = u < u_end;
+    if (!have) return;
+    const int tok0 = unit.t0 + t * kTile;
+    const int pi = tok0 / p.page_size;
+    slot0 = tok0 - pi * p.page_size;
+    page = ptx::ldg_keep(p.indices + unit.pbase + pi, keep);
+    ++t;
+  };
+  describe();
+
+  int it = 0;
+  while (have) {
+    const int s = it % kStages;
+    if (!wait_phase(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, abort)) {
+      if (lane == 0) give_up(p, abort);
+      break;
+    }
+    int pg = page;
+    if (static_cast<unsigned long long>(pg) >= static_cast<unsigned long long>(p.num_pages)) {
+      if (lane == 0) flag(p.image, PKD_DEVICE_BAD_PAGE);
+      pg = 0;
+    }
+    if (lane == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, G::kStageBytes);
+    __syncwarp();
+    // one box of (64 d, 16 slots, every head) per (tensor, d-half): the
+    // page tensors are seen as [page][head][slot][d] in either layout
+    if (lane < 4) {
+      const int tensor = lane >> 1, half = lane & 1;
+      const uint32_t dst = stage0 + s * G::kStageBytes + tensor * G::kTensorBytes +
+                           half * (HKV * kHalfBytes);
+      ptx::tma_load_4d_hint(dst, tensor ? map_v : map_k, half * 64, slot0, 0, pg,
+                            full0 + 8 * s, stream);
+    }
+    describe();
+    ++it;
   }
   // the CTA must not retire while this warp's copies are still landing
   for (int j = max(0, it - kStages); j < it; ++j)
@@ -728,20 +736,26 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// K or V pages with d innermost: NHD as [token row][head][d] (3-D), boxes of
-// 16 token rows x 1 head x 64 elements; HND as [page][head][slot][d] (4-D),
-// boxes of 64 elements x 16 slots x box_heads heads.  128-byte swizzle.
+// K or V pages with d innermost, 128-byte swizzle.
+//  * all_heads (the decode kernel): either layout seen as [page][head][slot]
+//    [d] (4-D; for NHD the slot stride is Hkv rows and the head stride one
+//    row), boxes of 64 elements x 16 slots x every head.
+//  * otherwise (the shared-prefix kernel): NHD as [token row][head][d] (3-D),
+//    HND as [page][head][slot][d] (4-D), boxes of 64 elements x 16 slots x
+//    one head.
 bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
-                  int page_size, int hkv, int layout, int box_heads) {
+                  int page_size, int hkv, int layout, bool all_heads) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return false;
   const cuuint64_t row = kRowBytes;
-  if (layout == PKD_LAYOUT_HND) {
+  if (layout == PKD_LAYOUT_HND || all_heads) {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim),
                           static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(hkv),
                           static_cast<cuuint64_t>(num_pages)};
-    cuuint64_t strides[3] = {row, row * page_size, row * page_size * hkv};
-    cuuint32_t box[4] = {64, kTile, static_cast<cuuint32_t>(box_heads), 1};
+    const bool hnd = layout == PKD_LAYOUT_HND;
+    cuuint64_t strides[3] = {hnd ? row : row * hkv, hnd ? row * page_size : row,
+                             row * page_size * hkv};
+    cuuint32_t box[4] = {64, kTile, static_cast<cuuint32_t>(all_heads ? hkv : 1), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -762,11 +776,12 @@ bool encode_pages(CUtensorMap *map, const void *base, long long num_pages,
 // Tensor maps of the last page pools seen (encoding is pure host work, but a
 // serving loop passes the same pools on every step).
 bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
-                 long long num_pages, int page_size, int hkv, int layout, int box_heads) {
+                 long long num_pages, int page_size, int hkv, int layout, bool all_heads) {
   struct Entry {
     const void *k, *v;
     long long num_pages;
-    int page_size, hkv, layout, box_heads;
+    int page_size, hkv, layout;
+    bool all_heads;
     CUtensorMap mk;
     CUtensorMap mv;
   };
@@ -776,14 +791,14 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
   std::lock_guard<std::mutex> lock(mutex);
   for (const Entry &e : cache)
     if (e.k == k && e.v == v && e.num_pages == num_pages && e.page_size == page_size &&
-        e.hkv == hkv && e.layout == layout && e.box_heads == box_heads && e.k) {
+        e.hkv == hkv && e.layout == layout && e.all_heads == all_heads && e.k) {
       *mk = e.mk;
       *mv = e.mv;
       return true;
     }
   Entry &e = cache[next];
-  if (!encode_pages(&e.mk, k, num_pages, page_size, hkv, layout, box_heads) ||
-      !encode_pages(&e.mv, v, num_pages, page_size, hkv, layout, box_heads)) {
+  if (!encode_pages(&e.mk, k, num_pages, page_size, hkv, layout, all_heads) ||
+      !encode_pages(&e.mv, v, num_pages, page_size, hkv, layout, all_heads)) {
     e.k = nullptr;
     return false;
   }
@@ -793,7 +808,7 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
   e.page_size = page_size;
   e.hkv = hkv;
   e.layout = layout;
-  e.box_heads = box_heads;
+  e.all_heads = all_heads;
   next = (next + 1) % 8;
   *mk = e.mk;
   *mv = e.mv;
@@ -805,7 +820,7 @@ bool cached_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
 bool page_tensor_maps(CUtensorMap *mk, CUtensorMap *mv, const void *k, const void *v,
                       long long num_pages, int page_size, int hkv, int layout) {
   // the shared-prefix kernel loads one head per box
-  return cached_maps(mk, mv, k, v, num_pages, page_size, hkv, layout, 1);
+  return cached_maps(mk, mv, k, v, num_pages, page_size, hkv, layout, false);
 }
 
 bool query_tensor_map(CUtensorMap *map, const void *q, int batch, int hq, int group) {
@@ -857,16 +872,21 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   // inside one page and token rows that fit in int32.
   const bool tiles_fit = a.page_size % kTile == 0 && a.num_pages > 0 &&
                          a.num_pages * static_cast<long long>(a.page_size) < (1ll << 31);
+  // automatic choice, measured: TMA boxes for HND pages (0.95 against 0.85
+  // of the copy peak on the batch-64 workload) and for NHD pages of 16
+  // tokens (batch-64 step -1.3%, cascade -4%); bulk rows for other NHD page
+  // sizes (64-token bf16 pages: TMA boxes 2% slower on the long-context
+  // workload) and for pages that do not hold whole tiles
   const bool want_tma =
       a.loader == PKD_LOADER_TMA_TILES ||
-      (a.loader == PKD_LOADER_AUTO && a.layout == PKD_LAYOUT_HND && tiles_fit);
+      (a.loader == PKD_LOADER_AUTO && tiles_fit &&
+       (a.layout == PKD_LAYOUT_HND || a.page_size == kTile));
   int loader = kLoaderBulk;
   if (want_tma) {
-    // HND boxes cover every head of a page's 16 slots (one box per tensor
-    // and d-half); NHD boxes one head
-    const int box_heads = a.layout == PKD_LAYOUT_HND ? a.num_kv_heads : 1;
+    // boxes cover every head of a page's 16 slots (one box per tensor and
+    // d-half)
     if (!tiles_fit || !cached_maps(&mk, &mv, a.k_pages, a.v_pages, a.num_pages,
-                                   a.page_size, a.num_kv_heads, a.layout, box_heads))
+                                   a.page_size, a.num_kv_heads, a.layout, true))
       return cudaErrorNotSupported;
     loader = kLoaderTma;
   }
