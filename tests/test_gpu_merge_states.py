@@ -32,7 +32,9 @@ def check(v, s, v_ref, s_ref, dtype):
     tol = {"f32": 1e-5, "f16": 2e-3, "bf16": 1.6e-2}[dtype]
     assert np.max(np.abs(v - v_ref)) <= tol
     fin = ~both_empty
-    assert np.max(np.abs(s[fin] - s_ref[fin])) <= 1e-4 * np.maximum(1, np.abs(s_ref[fin])).max()
+    if fin.any():
+        assert np.max(np.abs(s[fin] - s_ref[fin])) <= \
+            1e-4 * np.maximum(1, np.abs(s_ref[fin])).max()
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
@@ -88,3 +90,29 @@ def test_merge_states_rejects_bad_shapes():
     with pytest.raises(pkd.PkdError) as e:
         pkd.merge_states(v, s, v, s)
     assert e.value.status == -4
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_merge_states_random_shapes(seed):
+    """Seeded draws of n (0 included), heads, head_dim (multiples of 8 up to
+    1024), dtype, the share of empty states and the spread of s, each against
+    the oracle merge."""
+    rng = np.random.default_rng([9001, seed])
+    n = int(rng.choice([0, 1, 2, 7, 65, 300]))
+    h = int(rng.integers(1, 65))
+    d = 8 * int(rng.integers(1, 129))
+    dtype = ["f16", "bf16", "f32"][seed % 3]
+    empty = float(rng.choice([0.0, 0.1, 0.5, 1.0]))
+    va, sa = random_states(rng, n, h, d, dtype, empty)
+    vb, sb = random_states(rng, n, h, d, dtype, empty)
+    spread = float(rng.choice([1.0, 100.0, 1e4]))
+    sa = sa * spread / 20
+    sb = sb * spread / 20
+    out_v, out_s = pkd.merge_states(va.cuda(), sa.cuda(), vb.cuda(), sb.cuda())
+    torch.cuda.synchronize()
+    if n == 0:
+        assert out_v.numel() == 0 and out_s.numel() == 0
+        return
+    v_ref, s_ref = oracle.merge(va.double().numpy(), sa.double().numpy(),
+                                vb.double().numpy(), sb.double().numpy())
+    check(out_v, out_s, v_ref, s_ref, dtype)
