@@ -229,7 +229,7 @@ class Runner:
     """
 
     def __init__(self, wl, device, kv_loader=0, cascade="fused", layout="nhd",
-                 graph=False):
+                 graph=False, cascade_split=True):
         import torch
         import paged_kv_decode_plan_gb300 as pkd
         self.torch = torch
@@ -268,13 +268,29 @@ class Runner:
             qd.copy_(wl.q)
         self.q = self.qs[0]
         self.prefix = None
+        # fused cascade: the shared-prefix kernel (shared-memory / tensor bound)
+        # and the suffix decode (copy bound) run side by side on disjoint SMs:
+        # the prefix plan gets about 30% of the SMs in whole (head x row tile)
+        # groups, the suffix plan the rest, and the suffix decode, launched as
+        # a programmatic dependent, starts at once on the free SMs
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        prefix_ctas = suffix_ctas = 0
+        if self.fused and cascade_split:
+            group = wl.num_qo_heads // wl.num_kv_heads
+            base = wl.num_kv_heads * max(1, -(-wl.batch * group // 256))
+            prefix_ctas = base * max(1, round(0.3 * sms / base))
+            if prefix_ctas < sms:
+                suffix_ctas = sms - prefix_ctas
+            else:
+                prefix_ctas = 0
+        self.cascade_ctas = (prefix_ctas, suffix_ctas)
         if self.shared:
             pt = wl.extra_tables["prefix"]
             pages = pt.kv_indices[: pt.kv_indptr[1]].copy()
             prob = pkd.make_problem(batch=pt.batch, num_qo_heads=wl.num_qo_heads,
                                     num_kv_heads=wl.num_kv_heads, page_size=pt.page_size,
                                     dtype=wl.dtype, num_pages=wl.num_pages,
-                                    kv_layout=self.layout)
+                                    num_ctas=prefix_ctas, kv_layout=self.layout)
             self.prefix = dict(
                 pages=pages, last=int(pt.kv_last_page_len[0]),
                 ws=[pkd.PrefixWorkspace(prob, pages.size, device=device) for _ in range(2)],
@@ -285,6 +301,7 @@ class Runner:
                                     num_kv_heads=wl.num_kv_heads, page_size=t.page_size,
                                     dtype=wl.dtype, num_pages=wl.num_pages,
                                     min_chunks_per_request=wl.min_chunks_per_request,
+                                    num_ctas=suffix_ctas if self.fused else 0,
                                     kv_loader=kv_loader, kv_layout=self.layout)
             ws = [pkd.Workspace(prob, device=device) for _ in range(2)]
             # the three page-table arrays packed together after the queries in
@@ -585,7 +602,8 @@ def run_ours(args, ranks):
     device = torch.device("cuda", ranks.local)
     wl = make_workload(args)
     runner = Runner(wl, device, kv_loader={"auto": 0, "tma": 1, "bulk": 2}[args.loader],
-                    cascade=args.cascade, layout=args.layout, graph=args.graph == "on")
+                    cascade=args.cascade, layout=args.layout, graph=args.graph == "on",
+                    cascade_split=args.cascade_split == "on")
     stream = torch.cuda.current_stream()
 
     # host plan time (median of 20)
@@ -667,6 +685,7 @@ def run_ours(args, ranks):
         "kv_loader": args.loader,
         "kv_layout": args.layout,
         "cascade": (args.cascade if wl.name == "cascade" else None),
+        "cascade_ctas": (list(runner.cascade_ctas) if runner.fused else None),
         "prefix_us": (round(statistics.fmean(prefix_ms) * 1e3, 2)
                       if prefix_ms else None),
         "launch": "graph" if runner.use_graph else "eager",
@@ -848,6 +867,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--layout", choices=["nhd", "hnd"], default="nhd",
                     help="page tensor layout (the same values either way)")
+    ap.add_argument("--cascade-split", choices=["on", "off"], default="on",
+                    help="fused cascade: the prefix kernel and the suffix decode on "
+                         "disjoint SMs (about 30%% / 70%%) instead of one after the other")
     ap.add_argument("--cascade", choices=["fused", "shared", "per-request"],
                     default="fused",
                     help="cascade workload: shared-prefix kernel states folded into "
