@@ -4,19 +4,26 @@
 One step = one pass of the whole hot path over one synthetic batch: plan on
 the host (lengths -> split-KV work list -> H2D copy of the plan image), the
 decode kernel, and the split-KV merge kernel (by default replayed as one CUDA
-graph per workspace; ``--graph off`` launches them one by one).  The default workload is the
-64-request batch (lengths uniform on [128, 4096], Hq 32 / Hkv 8, head_dim 128,
-page_size 16, fp16); ``--workload`` selects another of
-paged_kv_decode_plan_gb300.workloads.  For the cascade workload a step plans
-the suffix table and the shared prefix and runs the shared-prefix kernel, the
-suffix decode and the cascade merge (``--cascade fused``, pkd_run_cascade's
-launches), or the prefix and suffix runs merged by merge_states
-(``--cascade shared``), or the prefix listed in every request's table
-(``--cascade per-request``).
+graph per workspace; ``--graph off`` launches them one by one).
+
+By default (``--workload all``) the five workloads of
+paged_kv_decode_plan_gb300.workloads are timed one after another with the
+same steps and warm-up: the single request, the 64-request batch, the
+256-request long tail, the cascade and, as the headline line, the
+long-context batch (8 x 131072 tokens, Hq 64 / Hkv 8, P 64, bf16, >= 132
+partial states per request + merge), the largest one that fits one GPU.  The
+other four are reported under ``per_config`` in the same line.
+``--workload NAME`` times one workload alone.  For the cascade workload a step
+plans the suffix table and the shared prefix and runs the shared-prefix
+kernel, the suffix decode and the cascade merge (``--cascade fused``,
+pkd_run_cascade's launches), or the prefix and suffix runs merged by
+merge_states (``--cascade shared``), or the prefix listed in every request's
+table (``--cascade per-request``).
 
 Rank 0 prints one JSON line.  Under torchrun every rank runs the same batch
 on its own GPU (weak scaling, no data-path collective); timing is the maximum
-over ranks.  ``--impl reference`` times the fp64 CPU oracle instead.
+over ranks.  ``--impl reference`` times the fp64 CPU oracle instead, on the
+headline workload.
 """
 from __future__ import annotations
 
@@ -50,6 +57,10 @@ DESCRIPTIONS = {
     "longctx": "long-context decode: 8 x 131072 tokens, Hq 64 / Hkv 8, D 128, P 64, bf16, "
                ">=132 partitions per request",
 }
+# "all" (the default) times the four others first and the long-context batch,
+# the largest configuration that fits one GPU, last, as the headline
+ALL_ORDER = ["single", "batch64", "longtail", "cascade", "longctx"]
+HEADLINE = "longctx"
 KERNEL_SOURCES = ["paged_kv_decode_plan_gb300/csrc/decode.cu",
                   "paged_kv_decode_plan_gb300/csrc/ptx.cuh",
                   "paged_kv_decode_plan_gb300/csrc/kernel_common.cuh"]
@@ -585,22 +596,66 @@ def pack_table(t):
     return np.concatenate([t.kv_indptr, t.kv_indices, t.kv_last_page_len]).astype(np.int32)
 
 
-def make_workload(args):
+def make_workload(args, name=None):
     from paged_kv_decode_plan_gb300 import workloads
+    name = name or (HEADLINE if args.workload == "all" else args.workload)
     if args.batch is None:
-        return workloads.WORKLOADS[args.workload]()
-    if args.workload not in ("longctx", "cascade"):
+        return workloads.WORKLOADS[name]()
+    if name not in ("longctx", "cascade"):
         raise SystemExit("--batch applies to the longctx and cascade workloads")
-    return workloads.WORKLOADS[args.workload](batch=args.batch)
+    return workloads.WORKLOADS[name](batch=args.batch)
 
 
 def run_ours(args, ranks):
+    """Every workload of ``args.workload`` ("all": the five), each timed
+    with the same steps and warm-up; returns rank 0's JSON line.  With
+    "all", the long-context batch is the headline and the other four go
+    into ``per_config``."""
     import torch
-    from paged_kv_decode_plan_gb300 import workloads
-
     torch.cuda.set_device(ranks.local)
     device = torch.device("cuda", ranks.local)
-    wl = make_workload(args)
+    names = ALL_ORDER if args.workload == "all" else [args.workload]
+    lines = {}
+    for name in names:
+        wl = make_workload(args, name)
+        lines[name] = measure(args, ranks, device, wl,
+                              cpu=(name == names[-1] or len(names) == 1))
+        del wl
+        torch.cuda.empty_cache()
+    line = lines[names[-1]]
+    if len(names) > 1:
+        line["per_config"] = {n: config_summary(lines[n]) for n in names[:-1]}
+        line["config"]["per_config"] = ("the other four workloads, each timed in this "
+                                        "run with the same steps and warm-up")
+    return line
+
+
+def config_summary(line):
+    """The figures of one workload's line that per_config reports."""
+    keys = ("us_per_batch", "value", "unit", "ms_per_step", "steps", "warmup",
+            "decode_us", "prefix_us", "host_enqueue_us_per_step", "total_gbs",
+            "plan_host_us", "num_units", "num_split_requests", "launch",
+            "gpu_launches", "dtype", "clocks")
+    out = {"workload": line["config"]["workload"],
+           "kv_bytes_per_step": line["config"]["kv_bytes_per_step"]}
+    out.update({k: line[k] for k in keys if k in line})
+    peak_key = [k for k in line if k.startswith("hbm_frac_of_")][0]
+    out["step_" + peak_key] = line[peak_key]
+    r = line["roofline"]
+    out["roofline"] = {"kernel": r["kernel"], "achieved": r["achieved"], "peak": r["peak"],
+                       "frac": r["frac"], "traffic": r["traffic"]}
+    out["e2e"] = {"us_per_batch": line["e2e"]["us_per_batch"],
+                  "value": line["e2e"]["value"], "unit": line["e2e"]["unit"]}
+    if line.get("cascade"):
+        out["cascade"] = line["cascade"]
+        out["cascade_ctas"] = line["cascade_ctas"]
+    return out
+
+
+def measure(args, ranks, device, wl, cpu):
+    """One workload: warm-up, pass 1 (whole steps), pass 2 (events around
+    each decode launch), end to end through the API; its JSON line."""
+    import torch
     runner = Runner(wl, device, kv_loader={"auto": 0, "tma": 1, "bulk": 2}[args.loader],
                     cascade=args.cascade, layout=args.layout, graph=args.graph == "on",
                     cascade_split=args.cascade_split == "on")
@@ -616,18 +671,20 @@ def run_ours(args, ranks):
                              part["table"].kv_last_page_len)
         plan_times.append(time.perf_counter() - t0)
 
-    for _ in range(args.warmup):
+    # first steps: eager, then (graph mode) capture and replay; the result
+    # and the device status word are checked before anything is timed
+    for _ in range(3):
         runner.step()
-    if runner.use_graph:   # capture (after >= 2 eager steps) and replay before timing
+    if runner.use_graph:
         for _ in range(3):
             runner.step()
     torch.cuda.synchronize()
     status = runner.status()
     if status:
-        raise RuntimeError("device status word %d after warm-up" % status)
+        raise RuntimeError("device status word %d after the first steps" % status)
     out, lse, _ = runner.result()
     if not bool(torch.isfinite(out).all()) or bool(torch.isnan(lse).any()):
-        raise RuntimeError("non-finite output after warm-up")
+        raise RuntimeError("non-finite output after the first steps")
 
     uuid = None
     try:
@@ -639,13 +696,19 @@ def run_ours(args, ranks):
               for _ in range(k)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(uuid) as clocks:
+        # the W warm-up steps run right before the timed region (the clock
+        # sampler's start-up pause would otherwise sit between them)
+        clocks.mark(0)
+        for _ in range(args.warmup):
+            runner.step()
         # pass 1: the whole step, start and end events only
         ranks.barrier()
         torch.cuda.synchronize()
-        clocks.mark(0)
         start.record(stream)
+        h0 = time.perf_counter()
         for _ in range(k):
             runner.step()
+        host_s = time.perf_counter() - h0
         end.record(stream)
         torch.cuda.synchronize()
         ranks.barrier()
@@ -679,6 +742,9 @@ def run_ours(args, ranks):
                            / 1e9, 2),
         "hbm_frac_of_%s" % peak_kind: round(agg["value_gbs"] / ranks.world / peak, 4),
         "decode_us": round(decode_mean_ms * 1e3, 2),
+        # host time to enqueue one step in pass 1 (plan + copies + launches);
+        # above us_per_batch the step is host-bound
+        "host_enqueue_us_per_step": round(host_s / k * 1e6, 2),
         "plan_host_us": round(statistics.median(plan_times) * 1e6, 1),
         "num_units": runner.parts[0]["plan"].num_units,
         "num_split_requests": runner.parts[0]["plan"].num_split_requests,
@@ -689,10 +755,11 @@ def run_ours(args, ranks):
         "prefix_us": (round(statistics.fmean(prefix_ms) * 1e3, 2)
                       if prefix_ms else None),
         "launch": "graph" if runner.use_graph else "eager",
-        "timing": "pass 1 (value, ms_per_step): K steps between two events; pass 2 "
-                  "(decode_us, roofline): the same K steps with events around each "
-                  "decode launch" + (" (inside the replayed graph, one step at a "
-                                     "time)" if runner.use_graph else ""),
+        "timing": "W warm-up steps right before pass 1; pass 1 (value, ms_per_step): K "
+                  "steps between two events; pass 2 (decode_us, roofline): the same K "
+                  "steps with events around each decode launch" +
+                  (" (inside the replayed graph, one step at a time)"
+                   if runner.use_graph else ""),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel",
                      "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
@@ -707,8 +774,9 @@ def run_ours(args, ranks):
         "gpu_launches": runner.launches_per_step * k,
         "clocks": clocks.summary(),
     }
-    if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
+    if cpu and ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+    del runner
     return line
 
 
@@ -863,7 +931,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(DESCRIPTIONS), default="batch64")
+    ap.add_argument("--workload", choices=["all"] + sorted(DESCRIPTIONS), default="all",
+                    help="all (default): every workload timed in one run, the "
+                         "long-context batch as the headline line and the others "
+                         "under per_config")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--layout", choices=["nhd", "hnd"], default="nhd",
                     help="page tensor layout (the same values either way)")

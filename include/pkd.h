@@ -276,17 +276,21 @@ pkd_status pkd_check_status(const void *int_ws_dev, uint32_t *device_status,
  * in a fixed __device__ array inside this library (256 KiB + 8 MiB, held by
  * every GPU that loads the library until the process exits).
  *
- * plan and host_image come from pkd_plan_host; the image is copied into the
+ * plan and host_image come from pkd_plan_host; host_image must hold at
+ * least plan->int_ws_bytes_used bytes, all of which are copied into the
  * array on `stream` (from pageable memory the call returns once the copy is
  * staged; pinned memory must stay untouched until the stream passes the
  * copy).  The other arguments are those of pkd_run.  A plan whose image
  * exceeds 262144 bytes or whose partial states exceed 8388608 bytes returns
  * PKD_ERR_WORKSPACE before any CUDA call; plan with a smaller
- * min_chunks_per_request or split the batch.  The first call on a device
- * looks up the array's address (with that device current); make it before
- * any stream capture.  All calls share the array: calls that overlap on the
- * GPU race.  Kernel range-check failures land in the array's copy of the
- * status word and are not reported.
+ * min_chunks_per_request or split the batch.  A call on a stream that is
+ * being captured returns PKD_ERR_UNSUPPORTED without launching anything.
+ * The first call on a device looks up the array's address (with that device
+ * current) and keeps it for the life of the process; make that call before
+ * any stream capture, and do not call this entry point on a device again
+ * after cudaDeviceReset on it.  All calls share the array: calls that
+ * overlap on the GPU race.  Kernel range-check failures land in the array's
+ * copy of the status word and are not reported.
  */
 pkd_status pkd_run_static(const pkd_plan_t *plan, const int32_t *host_image,
                           const void *q, const void *k_pages,

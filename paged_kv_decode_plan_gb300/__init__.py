@@ -312,6 +312,9 @@ def run_static(plan_: Plan, host_image, q, k_pages, v_pages, kv_indptr, kv_indic
         lse = torch.empty((p.batch, p.num_qo_heads), dtype=torch.float32,
                           device=q.device)
     image = np.ascontiguousarray(host_image, dtype=np.int32)
+    if image.nbytes < plan_.int_ws_bytes_used:
+        raise ValueError("host_image holds %d bytes; the plan image has %d"
+                         % (image.nbytes, plan_.int_ws_bytes_used))
     _check(load().pkd_run_static(
         ctypes.byref(plan_), _addr(image),
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_indptr), _ptr(kv_indices),

@@ -12,10 +12,15 @@
 //
 // The array's device address is looked up once per device (cudaGetSymbolAddress
 // with that device current) on the first call made on that device; make that
-// first call before any stream capture.  Every call shares the array: calls
-// whose work overlaps on the GPU (other streams, other threads) race on it.
-// Each call overwrites the plan image completely (its status word starts at
-// 0) and every partial slot a plan uses is written before it is read, so
+// first call before any stream capture.  The address is kept for the life of
+// the process: after cudaDeviceReset on a device, do not call this entry
+// point on that device again.  A call on a stream that is being captured is
+// refused (PKD_ERR_UNSUPPORTED): the plan image is copied from host memory by
+// each call and the kernels are bounded by that call's plan, which a captured
+// copy and launch would freeze.  Every call shares the array: calls whose
+// work overlaps on the GPU (other streams, other threads) race on it.  Each
+// call overwrites the plan image completely (its status word starts at 0)
+// and every partial slot a plan uses is written before it is read, so
 // nothing is left to clear between calls.
 #include <cuda_runtime.h>
 
@@ -82,15 +87,21 @@ extern "C" pkd_status pkd_run_static(const pkd_plan_t *plan,
                          std::to_string(plan->float_ws_bytes_needed) +
                          " bytes exceed the static limit of 8388608 bytes");
   if (plan->problem.batch == 0) return PKD_OK;
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capture);
+  if (e != cudaSuccess)
+    return pkd::fail(PKD_ERR_CUDA, std::string("cudaStreamIsCapturing: ") +
+                                       cudaGetErrorString(e));
+  if (capture != cudaStreamCaptureStatusNone)
+    return pkd::fail(PKD_ERR_UNSUPPORTED,
+                     "pkd_run_static is not supported on a capturing stream");
   void *base = nullptr;
   pkd_status st = scratch_address(&base);
   if (st != PKD_OK) return st;
   int32_t *image_d = static_cast<int32_t *>(base);
   float *partials_d = reinterpret_cast<float *>(image_d + kStaticImageWords);
-  cudaError_t e = cudaMemcpyAsync(image_d, host_image,
-                                  static_cast<size_t>(plan->int_ws_bytes_used),
-                                  cudaMemcpyHostToDevice,
-                                  static_cast<cudaStream_t>(stream));
+  e = cudaMemcpyAsync(image_d, host_image, static_cast<size_t>(plan->int_ws_bytes_used),
+                      cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return pkd::fail(PKD_ERR_CUDA, std::string("copying the plan image: ") +
                                        cudaGetErrorString(e));

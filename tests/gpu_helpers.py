@@ -11,6 +11,9 @@ Bounds (fp16 / bf16 inputs, fp32 accumulation):
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -77,6 +80,18 @@ def half_ulp(x, dtype):
     return 0.5 * np.exp2(e - (bits - 1))
 
 
+def log_accuracy(summary, dtype):
+    """Appends a comparison's error summary, with the test that made it, to
+    the JSON-lines file named by PKD_ACCURACY_LOG (if set)."""
+    path = os.environ.get("PKD_ACCURACY_LOG")
+    if not path:
+        return
+    rec = dict(summary, dtype=dtype,
+               test=os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0])
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
+
+
 def compare(out, lse, ref_out, ref_lse, dtype, rows=None):
     """Checks GPU (out, lse) against the oracle; returns an error summary."""
     o = out.float().cpu().numpy().astype(np.float64)
@@ -103,7 +118,10 @@ def compare(out, lse, ref_out, ref_lse, dtype, rows=None):
     lse_bound = LSE_TOL + 2.0 * np.spacing(np.abs(rs).astype(np.float32)).astype(np.float64)
     summary.update(max_err_out=float(err.max()),
                    max_err_out_small=float(err[~large].max()) if (~large).any() else 0.0,
-                   max_err_lse=float(lse_err.max()), n_large=int(large.sum()))
+                   max_err_out_large=float(err[large].max()) if large.any() else 0.0,
+                   max_err_lse=float(lse_err.max()), n_large=int(large.sum()),
+                   n_elements=int(err.size))
+    log_accuracy(summary, dtype)
     worst = np.unravel_index(np.argmax(err - bound), err.shape)
     assert np.all(err <= bound), "out error %.3g at %s (ref %.4g)" % (
         err[worst], worst, ro[worst])

@@ -55,6 +55,48 @@ def test_static_entry_matches_workspace_entry_twice():
         gh.compare(out_s, lse_s, ref_out, ref_lse, wl.dtype)
 
 
+def test_static_entry_allocates_no_device_memory():
+    """A warm call with caller-given out / lse leaves both torch's allocator
+    and the device's free memory as they were."""
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device")
+    ctas = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = _batch(23, [2000, 5, 700], "f16", 32)
+    dev = gh.DeviceBatch(wl)
+    t = wl.table
+    prob = pkd.make_problem(batch=t.batch, num_qo_heads=wl.num_qo_heads,
+                            num_kv_heads=wl.num_kv_heads, page_size=t.page_size,
+                            dtype=wl.dtype, num_pages=wl.num_pages, num_ctas=ctas)
+    plan, image = pkd.plan_host(prob, t.kv_indptr, t.kv_last_page_len, t.kv_indices)
+    assert plan.num_split_requests > 0
+    indptr, indices, last = gh.device_table(t)
+    out = torch.empty(t.batch, wl.num_qo_heads, 128, dtype=dev.q.dtype, device="cuda")
+    lse = torch.empty(t.batch, wl.num_qo_heads, dtype=torch.float32, device="cuda")
+    args = (plan, image, dev.q, dev.k, dev.v, indptr, indices, last, wl.sm_scale)
+    pkd.run_static(*args, out=out, lse=lse)        # warm: address looked up
+    torch.cuda.synchronize()
+    first = out.clone(), lse.clone()
+    torch.cuda.synchronize()
+    allocated = torch.cuda.memory_allocated()
+    free_before, _ = torch.cuda.mem_get_info()
+    pkd.run_static(*args, out=out, lse=lse)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == allocated
+    assert free_after == free_before
+    assert torch.equal(out, first[0]) and torch.equal(lse, first[1])
+
+
+def test_static_entry_rejects_short_host_image():
+    prob = pkd.make_problem(batch=2, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                            dtype="f16", num_pages=64, num_ctas=152)
+    table = workloads.table_from_lengths([300, 40], 16, np.arange(64))
+    plan, image = pkd.plan_host(prob, table.kv_indptr, table.kv_last_page_len)
+    q = torch.empty(2, 32, 128, dtype=torch.float16, device="cuda")
+    with pytest.raises(ValueError):
+        pkd.run_static(plan, image[:-1], q, q, q, q, q, q, 0.1)
+
+
 def test_static_entry_rejects_plans_beyond_its_limit():
     # 8 requests x 2000 pieces of 64 query heads: ~16 000 partial slots,
     # far beyond the 8 MiB of partial states the static array holds
