@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define PKD_ABI_VERSION 4
+#define PKD_ABI_VERSION 5
 
 typedef enum {
   PKD_OK = 0,
@@ -358,10 +358,25 @@ pkd_status pkd_prefix_workspace_size(const pkd_problem *problem,
                                      size_t *int_ws_bytes, size_t *float_ws_bytes,
                                      size_t *staging_bytes);
 
-/* Validates the prefix page list on the host (ids in [0, num_pages),
- * 1 <= last_page_len <= page_size), chooses the chunking, writes the prefix
- * plan image (header + page ids) into pinned_staging and copies it into
- * int_ws_dev on `stream`. */
+/* Plans a shared prefix on the host only (no CUDA call; [W] "Plan and run"):
+ * validates the prefix page list (ids in [0, num_pages), 1 <= last_page_len
+ * <= page_size), chooses the chunking and writes the prefix plan image
+ * (a 16-word header, then the page ids) to host_image.  Chunking: per
+ * key/value head the batch x g query rows form row_tiles = ceil(rows / 256)
+ * tiles; the prefix, walked in 64-token steps, is cut into as many equal
+ * pieces (chunks of chunk_tiles steps) as fit (Hkv x row_tiles) x chunks <=
+ * num_ctas, at least one.  problem->num_ctas must be explicit (> 0).
+ * Errors: PKD_ERR_INVALID_ARG, PKD_ERR_PAGE_TABLE, PKD_ERR_UNSUPPORTED,
+ * PKD_ERR_WORKSPACE (image larger than host_image_bytes). */
+pkd_status pkd_plan_shared_prefix_host(const pkd_problem *problem,
+                                       const int32_t *prefix_pages_h,
+                                       int32_t prefix_num_pages,
+                                       int32_t prefix_last_page_len,
+                                       pkd_prefix_plan_t *plan, int32_t *host_image,
+                                       size_t host_image_bytes);
+
+/* pkd_plan_shared_prefix_host into pinned_staging, then one asynchronous
+ * copy of the image into int_ws_dev on `stream`. */
 pkd_status pkd_plan_shared_prefix(const pkd_problem *problem,
                                   const int32_t *prefix_pages_h,
                                   int32_t prefix_num_pages,

@@ -5,9 +5,12 @@
 i belongs to request ``batch_indices[i]`` at position ``positions[i]`` of that
 request; the page table already covers the request's new length; the token's
 key and value rows (all heads) go to page ``kv_indices[kv_indptr[b] + t // P]``,
-slot ``t % P`` of the NHD page tensors.  Pinned by tests/test_append_ref.py:
-every appended token reads back through the page table unchanged, and the
-result does not depend on the order of the new tokens.
+slot ``t % P`` of the NHD page tensors ([pages][P][Hkv][D]), or of the HND
+ones ([pages][Hkv][P][D], "KV-Cache Layout in FlashInfer", "Layout:
+NHD/HND").  Pinned by tests/test_append_ref.py: every appended token reads
+back through the page table unchanged, the result does not depend on the
+order of the new tokens, and appending into HND pools gives exactly the HND
+transpose of appending into the same NHD pools.
 """
 from __future__ import annotations
 

@@ -11,7 +11,8 @@ Entry points (same names as the C ABI without the ``pkd_`` prefix):
 ``pkd_run``, ``pkd_run_decode``, ``pkd_run_merge`` or
 ``pkd_run_decode_states``), ``run_static``, ``merge_states``,
 ``check_status``, the shared-prefix calls (``plan_shared_prefix``,
-``run_shared_prefix``, ``run_shared_prefix_states``, ``run_cascade``,
+``plan_shared_prefix_host``, ``run_shared_prefix``, ``run_shared_prefix_states``,
+``run_cascade``,
 ``run_cascade_merge``), ``append_kv``, plus :class:`Workspace` and
 :class:`PrefixWorkspace`, which allocate the buffers a capacity needs.
 """
@@ -33,7 +34,7 @@ STATUS_NAMES = {0: "PKD_OK", -1: "PKD_ERR_INVALID_ARG", -2: "PKD_ERR_PAGE_TABLE"
                 -3: "PKD_ERR_WORKSPACE", -4: "PKD_ERR_UNSUPPORTED",
                 -5: "PKD_ERR_CUDA", -6: "PKD_ERR_DEVICE_CHECK"}
 
-ABI_VERSION = 4  # PKD_ABI_VERSION of include/pkd.h
+ABI_VERSION = 5  # PKD_ABI_VERSION of include/pkd.h
 
 # every symbol include/pkd.h declares
 EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
@@ -41,7 +42,8 @@ EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
             "pkd_run_merge", "pkd_merge_states", "pkd_check_status",
             "pkd_run_static", "pkd_prefix_workspace_size", "pkd_plan_shared_prefix",
             "pkd_run_shared_prefix", "pkd_append_kv", "pkd_run_shared_prefix_states",
-            "pkd_run_cascade", "pkd_run_cascade_merge", "pkd_run_decode_states")
+            "pkd_run_cascade", "pkd_run_cascade_merge", "pkd_run_decode_states",
+            "pkd_plan_shared_prefix_host")
 
 
 class PkdError(RuntimeError):
@@ -122,6 +124,10 @@ def load():
     lib.pkd_plan_shared_prefix.argtypes = [ctypes.POINTER(Problem), i32p, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.POINTER(PrefixPlan),
                                            vp, ctypes.c_size_t, vp, ctypes.c_size_t, vp]
+    lib.pkd_plan_shared_prefix_host.argtypes = [ctypes.POINTER(Problem), i32p,
+                                                ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.POINTER(PrefixPlan), i32p,
+                                                ctypes.c_size_t]
     lib.pkd_run_shared_prefix.argtypes = [ctypes.POINTER(PrefixPlan), vp, vp, vp, vp, vp,
                                           ctypes.c_size_t, ctypes.c_float, vp, vp, vp]
     lib.pkd_run_shared_prefix_states.argtypes = [ctypes.POINTER(PrefixPlan), vp, vp, vp,
@@ -379,6 +385,21 @@ def prefix_workspace_size(problem: Problem, max_prefix_pages: int):
                                             ctypes.byref(a), ctypes.byref(b),
                                             ctypes.byref(c)))
     return a.value, b.value, c.value
+
+
+def plan_shared_prefix_host(problem: Problem, prefix_pages, prefix_last_page_len):
+    """Host-only prefix planning; returns (PrefixPlan, image as an int32 array)."""
+    prob = Problem.from_buffer_copy(problem)
+    if prob.num_ctas <= 0:
+        raise ValueError("plan_shared_prefix_host needs an explicit num_ctas")
+    pages, p_pages = _host_i32(prefix_pages)
+    n = 0 if prefix_pages is None else int(np.asarray(prefix_pages).size)
+    image = np.zeros(16 + n + 1, dtype=np.int32)
+    out = PrefixPlan()
+    _check(load().pkd_plan_shared_prefix_host(
+        ctypes.byref(prob), p_pages, n, int(prefix_last_page_len), ctypes.byref(out),
+        _addr(image), image.nbytes))
+    return out, image[: out.int_ws_bytes_used // 4].copy()
 
 
 def plan_shared_prefix(problem: Problem, prefix_pages, prefix_last_page_len, *,

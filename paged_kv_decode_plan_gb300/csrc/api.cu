@@ -411,6 +411,18 @@ pkd_status pkd_prefix_workspace_size(const pkd_problem *problem,
   return PKD_OK;
 }
 
+pkd_status pkd_plan_shared_prefix_host(const pkd_problem *problem,
+                                       const int32_t *prefix_pages_h,
+                                       int32_t prefix_num_pages,
+                                       int32_t prefix_last_page_len,
+                                       pkd_prefix_plan_t *plan, int32_t *host_image,
+                                       size_t host_image_bytes) {
+  pkd::clear_error();
+  if (!problem) return fail(PKD_ERR_INVALID_ARG, "null problem");
+  return pkd::plan_prefix_impl(*problem, prefix_pages_h, prefix_num_pages,
+                               prefix_last_page_len, plan, host_image, host_image_bytes);
+}
+
 pkd_status pkd_plan_shared_prefix(const pkd_problem *problem,
                                   const int32_t *prefix_pages_h,
                                   int32_t prefix_num_pages,

@@ -25,7 +25,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version():
-    assert pkd.abi_version() == 4 == pkd.ABI_VERSION
+    assert pkd.abi_version() == 5 == pkd.ABI_VERSION
 
 
 def test_struct_sizes_match_c_layout():

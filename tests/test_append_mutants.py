@@ -19,11 +19,18 @@ MUTANTS = {
     "past-the-end token kept": ("t >= lengths[b]", "t > lengths[b]"),
     "V written with K": ("v[page, t % page_size] = v_new[i]", "v[page, t % page_size] = k_new[i]"),
     "page index from the slot": ("+ t // page_size])", "+ t % page_size])"),
+    "HND: slot and head swapped": ("k[page, :, t % page_size] = k_new[i]",
+                                   "k[page, t % page_size, :] = k_new[i]"),
+    "HND: slot from the page index": ("k[page, :, t % page_size] = k_new[i]",
+                                      "k[page, :, t // page_size] = k_new[i]"),
+    "HND: page size from the head axis": ("page_size = k.shape[2] if layout",
+                                          "page_size = k.shape[1] if layout"),
 }
 
 PINS = [pins.test_appended_rows_read_back_and_others_are_untouched,
         pins.test_append_order_does_not_matter_and_out_of_range_is_skipped,
-        pins.test_appended_token_is_what_its_request_attends_to]
+        pins.test_appended_token_is_what_its_request_attends_to,
+        pins.test_hnd_append_is_the_transpose_of_nhd_append]
 
 
 def _mutated(old, new):

@@ -2,7 +2,12 @@
 
 Appending writes through the page table, so the facts fixed outside it are:
 each appended row reads back through the same table unchanged, rows not
-appended are untouched, and the order of the new tokens does not matter.
+appended are untouched, and the order of the new tokens does not matter.  The
+HND branch is pinned to the NHD one: the two layouts hold the same values
+with the slot and head axes exchanged ("Welcome to FlashInfer's
+documentation!", "KV-Cache Layout in FlashInfer", "Layout: NHD/HND"), so
+appending into HND pools must give, bit for bit, the HND transpose of
+appending into the same NHD pools.
 """
 import numpy as np
 
@@ -92,3 +97,34 @@ def test_appended_token_is_what_its_request_attends_to():
             assert np.max(np.abs(out[b, h] - vn[i, h // g])) <= 1e-12
     for h in range(hkv * g):   # request 4 got no token
         assert min(np.max(np.abs(out[4, h] - vn[i, h // g])) for i in range(bi.size)) > 0.1
+
+
+def _hnd(x):
+    """NHD [pages, P, Hkv, D] -> HND [pages, Hkv, P, D] (the same values)."""
+    return np.ascontiguousarray(np.swapaxes(x, 1, 2))
+
+
+def test_hnd_append_is_the_transpose_of_nhd_append():
+    # page sizes above, equal to and below Hkv, so a slot / head mix-up
+    # cannot hide behind equal axis lengths
+    for seed, (lengths, page, hkv) in enumerate([([5, 17, 1, 0, 33], 4, 2),
+                                                 ([40, 9, 64], 16, 4),
+                                                 ([7, 12, 3], 3, 3),
+                                                 ([9, 2], 1, 8)]):
+        rng = np.random.default_rng(100 + seed)
+        k, v, indptr, indices, last = _case(rng, lengths, page, hkv)
+        n = 12
+        bi = rng.integers(0, len(lengths), n).astype(np.int32)
+        pos = np.array([rng.integers(0, max(lengths[b], 1)) for b in bi], np.int32)
+        pos[0] = 10_000   # one token past its request's end: skipped either way
+        _, keep = np.unique(bi.astype(np.int64) * 100_000 + pos, return_index=True)
+        bi, pos = bi[keep], pos[keep]
+        kn = rng.standard_normal((bi.size, hkv, 8)).astype(np.float32)
+        vn = rng.standard_normal((bi.size, hkv, 8)).astype(np.float32)
+        k_nhd, v_nhd, skip_nhd = append_ref.append_kv(k, v, kn, vn, bi, pos, indptr,
+                                                      indices, last)
+        k_hnd, v_hnd, skip_hnd = append_ref.append_kv(_hnd(k), _hnd(v), kn, vn, bi, pos,
+                                                      indptr, indices, last, layout="HND")
+        assert skip_hnd == skip_nhd and len(skip_nhd) >= 1
+        assert k_hnd.shape == _hnd(k).shape
+        assert np.array_equal(k_hnd, _hnd(k_nhd)) and np.array_equal(v_hnd, _hnd(v_nhd))

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import paged_kv_decode_plan_gb300 as pkd
+from oracle import prefix_plan_ref
 from paged_kv_decode_plan_gb300 import workloads
 from tests import gpu_helpers as gh
 
@@ -67,6 +68,27 @@ def test_shared_prefix_matches_oracle(case):
     assert plan.prefix_len == length and plan.chunks >= 1
     ref_out, ref_lse = gh.oracle_ref(wl, table=table)
     gh.compare(out, lse, ref_out, ref_lse, dtype)
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_device_prefix_image_matches_restatement(case):
+    """The image pkd_plan_shared_prefix copies to the device equals, byte for
+    byte, the plain-Python restatement of the prefix planning rule."""
+    batch, hq, hkv, page, length, dtype, ctas = case
+    wl, pages, last, _ = _prefix_case(batch, hq, hkv, page, length, dtype,
+                                      seed=batch * 7 + length)
+    prob = pkd.make_problem(batch=wl.batch, num_qo_heads=hq, num_kv_heads=hkv,
+                            page_size=page, dtype=dtype, num_pages=wl.num_pages,
+                            num_ctas=ctas)
+    pws = pkd.PrefixWorkspace(prob, max(1, pages.size))
+    plan = pws.plan(pages, last)
+    torch.cuda.synchronize()
+    img = pws.int_ws[: plan.int_ws_bytes_used].cpu().numpy().view(np.int32)
+    num_ctas = ctas or torch.cuda.get_device_properties(0).multi_processor_count
+    scalars, ref_img = prefix_plan_ref.plan(batch, hq, hkv, page, pages, last, num_ctas)
+    assert img.tobytes() == ref_img.tobytes()
+    for key, value in scalars.items():
+        assert getattr(plan, key) == value, key
 
 
 def test_shared_prefix_rejects_bad_pages_and_page_sizes():
