@@ -47,6 +47,7 @@ METRIC = ("paged decode attention µs/batch and KV GB/s as fraction of "
           "GB300 HBM peak")
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
+GRAPH_COPIES_MAX_KV = 64 * 1024 * 1024
 DESCRIPTIONS = {
     "single": "single-request decode: 1 x 512 tokens, Hq 32 / Hkv 8, D 128, P 16, fp16",
     "batch64": "batch 64 decode: lengths U[128,4096], Hq 32 / Hkv 8, D 128, P 16, fp16",
@@ -228,19 +229,24 @@ class ClockSampler:
 class Runner:
     """Device-resident batch plus workspaces; one `step()` = plan + run.
 
-    Serving-loop pipelining: two workspaces per table alternate between
-    steps, and each step's plan image is copied on a side stream while the
-    previous step still runs; the decode launch waits only for its own copy.
-    With ``graph``, the kernel launches of a step are one CUDA graph per
-    workspace (captured after the eager warm-up, valid for every later plan of
-    the same capacity); planning and the plan copies stay on the host per step.
-    Queries, device page tables and outputs are also kept per workspace turn,
-    so a step's input copies and the previous step's read-back can overlap the
-    running step (the end-to-end loop).
+    Two workspaces per table alternate between steps (turns), each with its
+    own queries, device page tables and outputs.  Two schedules for the
+    copies of a step:
+
+    * ``side``: pkd_plan copies each plan image on a side stream while the
+      previous step still runs (end to end, the input copy joins it and the
+      read-back runs on a third stream), so the copies overlap the
+      neighbouring steps' kernels; the kernels of a turn are one CUDA graph
+      (``--graph on``, after two eager steps) or separate launches.
+    * ``graph``: the host plans into the turn's pinned staging buffer and
+      replays one CUDA graph holding the plan-image copy (pkd_copy_plan: a
+      kernel that reads the pinned image, its size from its header), the
+      input copy and read-back (end to end) and the kernels: the fewest host
+      calls per step, but the copies no longer overlap other steps' kernels.
     """
 
     def __init__(self, wl, device, kv_loader=0, cascade="fused", layout="nhd",
-                 graph=False, cascade_split=True):
+                 graph=False, cascade_split=True, copies="side"):
         import torch
         import paged_kv_decode_plan_gb300 as pkd
         self.torch = torch
@@ -327,6 +333,11 @@ class Runner:
             outs = [self._pair() for _ in range(2)]
             self.parts.append(dict(table=t, ws=ws, devs=devs, packs=packs, outs=outs))
         self.finals = [self._pair() for _ in range(2)]
+        # graph mode plans on the host (num_ctas must be explicit)
+        for part in self.parts:
+            part["problem"] = _explicit(part["ws"][0].problem, self)
+        if self.prefix is not None:
+            self.prefix["problem"] = _explicit(self.prefix["ws"][0].problem, self)
         self.copy_stream = torch.cuda.Stream(device)
         self.read_stream = torch.cuda.Stream(device)
         # per-turn events, created once and re-recorded every step
@@ -339,6 +350,7 @@ class Runner:
         self.turn = 0
         self.launches_per_step = 0
         self.use_graph = graph
+        self.copies = copies if graph else "side"
         self.eager_steps = 0
         self.graphs = {}
         # timing events inside a graph must be real event-record nodes
@@ -366,9 +378,101 @@ class Runner:
 
     def step(self, events=None, inputs=None, outputs=None):
         """One step on workspace turn i.  ``inputs`` (a pinned copy of the input
-        buffer: queries and packed page tables) is copied in on the copy stream;
-        ``outputs`` (a pinned buffer the size of a result pair's) receives the
-        step's (out, lse) on the read-back stream."""
+        buffer: queries and packed page tables) is copied in before the
+        kernels; ``outputs`` (a pinned buffer the size of a result pair's)
+        receives the step's (out, lse).  Graph mode (after two eager steps):
+        the host plans into the turn's pinned staging buffer(s) and replays one
+        graph holding the plan-image copies, the input copy (end to end), the
+        kernels and the read-back (end to end)."""
+        timed_in_graph = events is None or self.timing_events is not None
+        graph = self.use_graph and self.eager_steps >= 2 and timed_in_graph
+        if graph and self.copies == "graph":
+            self._step_graph(events, inputs, outputs)
+        else:
+            self._step_side(events, inputs, outputs, graph)
+            if not graph:
+                self.eager_steps += 1
+
+    def _plan_graph(self, i):
+        """Host planning of turn i into its pinned staging buffer(s); the
+        turn's graph copies them to the device."""
+        for part in self.parts:
+            t = part["table"]
+            part["plan"], _ = self.pkd.plan_host(part["problem"], t.kv_indptr,
+                                                 t.kv_last_page_len,
+                                                 image=part["ws"][i].staging[0])
+        if self.prefix is not None:
+            pre = self.prefix
+            pre["plan"], _ = self.pkd.plan_shared_prefix_host(
+                pre["problem"], pre["pages"], pre["last"], image=pre["ws"][i].staging)
+
+    def _step_graph(self, events, inputs, outputs):
+        torch = self.torch
+        i = self.turn
+        self.turn ^= 1
+        self.last_turn = i
+        # the turn's previous graph must have read its staging buffers
+        if self.done[i] is not None:
+            self.done[i].synchronize()
+        self._plan_graph(i)
+        key = (i, events is not None, inputs is not None)
+        if key not in self.graphs:
+            self._capture(i, events is not None, inputs, outputs)
+        self.graphs[key].replay()
+        done = self.done_ev[i]
+        done.record(torch.cuda.current_stream())
+        self.done[i] = done
+        if events is not None:
+            torch.cuda.synchronize()
+            e = self.timing_events
+            self.timings.append((e[0].elapsed_time(e[1]),
+                                 e[2].elapsed_time(e[3]) if self.prefix else None))
+
+    def _capture(self, i, timed, inputs, outputs):
+        """The graph of turn i: plan-image copies from the turn's pinned
+        staging (pkd_copy_plan, which reads each image's size when it runs,
+        so any later plan of the capacity fits), [input copy], the kernels,
+        [read-back]."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            # the input copy (copy engine) first, then only kernels until the
+            # read-back: one engine hand-off each way
+            if inputs is not None:
+                self.inbufs[i].copy_(inputs, non_blocking=True)
+            # pkd_copy_plan: a kernel reads each pinned image (its current
+            # size from its header) into the workspace
+            for part in self.parts:
+                ws = part["ws"][i]
+                self.pkd.copy_plan(ws.staging[0], ws.int_ws)
+            if self.prefix is not None:
+                ws = self.prefix["ws"][i]
+                self.pkd.copy_plan(ws.staging, ws.int_ws)
+            self._launch(i, self.timing_events if timed else None)
+            if outputs is not None:
+                outputs.copy_(self.result_turn(i)[2], non_blocking=True)
+        torch.cuda.synchronize()
+        self.graphs[(i, timed, inputs is not None)] = g
+        # graph launches of this step: the kernels of _launch (copies are not
+        # counted as kernels)
+
+    def _capture_kernels(self, i, timed):
+        """Turn i's kernel launches as one graph (valid for every later plan
+        of the workspace's capacity)."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._launch(i, self.timing_events if timed else None)
+        torch.cuda.synchronize()
+        self.graphs[(i, timed, "kernels")] = g
+
+    def _step_side(self, events=None, inputs=None, outputs=None, graph=False):
+        """Copies beside the kernels: plan (pkd_plan copies the image on the
+        copy stream), input copy on the copy stream, the kernels on the main
+        stream (one kernel-only graph per turn with ``graph``), read-back on
+        its own stream."""
         torch = self.torch
         main = torch.cuda.current_stream()
         i = self.turn
@@ -392,11 +496,11 @@ class Runner:
         main.wait_event(ready)
         if self.read[i] is not None:   # this turn's previous outputs were read back
             main.wait_event(self.read[i])
-        timed_in_graph = events is None or self.timing_events is not None
-        if self.use_graph and self.eager_steps >= 2 and timed_in_graph:
-            if not self.graphs:
-                self._capture()
-            self.graphs[(i, events is not None)].replay()
+        if graph:
+            key = (i, events is not None, "kernels")
+            if key not in self.graphs:
+                self._capture_kernels(i, events is not None)
+            self.graphs[key].replay()
             if events is not None:
                 torch.cuda.synchronize()
                 e = self.timing_events
@@ -404,7 +508,6 @@ class Runner:
                                      e[2].elapsed_time(e[3]) if self.prefix else None))
         else:
             self._launch(i, events)
-            self.eager_steps += 1
         done = self.done_ev[i]
         done.record(main)
         self.done[i] = done
@@ -416,18 +519,6 @@ class Runner:
             rd = self.read_ev[i]
             rd.record(self.read_stream)
             self.read[i] = rd
-
-    def _capture(self):
-        """One graph per workspace, plain and with timing events."""
-        torch = self.torch
-        torch.cuda.synchronize()
-        for i in (0, 1):
-            for timed in ((False, True) if self.timing_events is not None else (False,)):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    self._launch(i, self.timing_events if timed else None)
-                self.graphs[(i, timed)] = g
-        torch.cuda.synchronize()
 
     def _launch(self, i, events=None):
         """The kernel launches of one step on the current stream."""
@@ -500,8 +591,11 @@ class Runner:
         return dec, pre
 
     def result(self):
-        """(out, lse) of the last step."""
-        i = self.last_turn
+        """(out, lse, buffer) of the last step."""
+        return self.result_turn(self.last_turn)
+
+    def result_turn(self, i):
+        """(out, lse, buffer) of workspace turn i."""
         if len(self.parts) == 2 or self.prefix is not None:
             return self.finals[i]
         return self.parts[0]["outs"][i]
@@ -634,7 +728,7 @@ def config_summary(line):
     """The figures of one workload's line that per_config reports."""
     keys = ("us_per_batch", "value", "unit", "ms_per_step", "steps", "warmup",
             "decode_us", "prefix_us", "host_enqueue_us_per_step", "total_gbs",
-            "plan_host_us", "num_units", "num_split_requests", "launch",
+            "plan_host_us", "num_units", "num_split_requests", "launch", "copies",
             "gpu_launches", "dtype", "clocks")
     out = {"workload": line["config"]["workload"],
            "kv_bytes_per_step": line["config"]["kv_bytes_per_step"]}
@@ -656,9 +750,15 @@ def measure(args, ranks, device, wl, cpu):
     """One workload: warm-up, pass 1 (whole steps), pass 2 (events around
     each decode launch), end to end through the API; its JSON line."""
     import torch
+    copies = args.copies
+    if copies == "auto":
+        # a step that moves little KV is bound by launch and copy latency and
+        # by host calls: one graph per step; a bandwidth-bound step hides its
+        # copies behind the neighbouring steps' kernels
+        copies = "graph" if workload_kv_bytes(wl) <= GRAPH_COPIES_MAX_KV else "side"
     runner = Runner(wl, device, kv_loader={"auto": 0, "tma": 1, "bulk": 2}[args.loader],
                     cascade=args.cascade, layout=args.layout, graph=args.graph == "on",
-                    cascade_split=args.cascade_split == "on")
+                    cascade_split=args.cascade_split == "on", copies=copies)
     stream = torch.cuda.current_stream()
 
     # host plan time (median of 20)
@@ -754,7 +854,8 @@ def measure(args, ranks, device, wl, cpu):
         "cascade_ctas": (list(runner.cascade_ctas) if runner.fused else None),
         "prefix_us": (round(statistics.fmean(prefix_ms) * 1e3, 2)
                       if prefix_ms else None),
-        "launch": "graph" if runner.use_graph else "eager",
+        "launch": ("graph" if runner.use_graph else "eager"),
+        "copies": runner.copies,
         "timing": "W warm-up steps right before pass 1; pass 1 (value, ms_per_step): K "
                   "steps between two events; pass 2 (decode_us, roofline): the same K "
                   "steps with events around each decode launch" +
@@ -793,10 +894,11 @@ def run_e2e(args, runner, device, ranks):
     """Same metric through the public API: every step copies its inputs
     (queries and page table) host-to-device from pinned memory, plans, runs,
     and copies out and lse device-to-host into one of two pinned buffers.
-    The copies run on their own streams and overlap the neighbouring steps'
-    kernels (each turn's device buffers are reused only after their read-back
-    completed), as a serving loop would overlap them; the timed region ends
-    with a synchronise after the last read-back."""
+    Graph mode: the copies are nodes of the step's graph, before and after
+    its kernels.  Eager mode: they run on their own streams and overlap the
+    neighbouring steps' kernels (each turn's device buffers are reused only
+    after their read-back completed).  The timed region ends with a
+    synchronise after the last read-back."""
     import torch
     wl = runner.wl
     in_h = runner.host_inputs()
@@ -805,17 +907,17 @@ def run_e2e(args, runner, device, ranks):
     h2d = in_h.numel()
     d2h = res_bytes
     steps = max(3, min(args.steps, args.e2e_steps))
-    turn = [0]
 
     def one():
-        i = turn[0]
-        turn[0] ^= 1
-        runner.step(inputs=in_h, outputs=outs_h[i])
+        # each workspace turn reads back into its own pinned buffer
+        runner.step(inputs=in_h, outputs=outs_h[runner.turn])
 
     for _ in range(3):
         one()
     torch.cuda.synchronize()
     image_bytes = sum(int(p["plan"].int_ws_bytes_used) for p in runner.parts)
+    if runner.prefix is not None:
+        image_bytes += int(runner.prefix["plan"].int_ws_bytes_used)
 
     ranks.barrier()
     t0 = time.perf_counter()
@@ -824,7 +926,7 @@ def run_e2e(args, runner, device, ranks):
     torch.cuda.synchronize()
     elapsed = time.perf_counter() - t0
     # the last read-back holds the last step's device result
-    if not torch.equal(outs_h[turn[0] ^ 1], runner.result()[2].cpu()):
+    if not torch.equal(outs_h[runner.last_turn], runner.result()[2].cpu()):
         raise RuntimeError("read-back differs from the device result")
     agg = aggregate(ranks, runner.kv_bytes(), elapsed, steps)
     return {"value": round(agg["value_gbs"], 2), "unit": "GB/s",
@@ -957,6 +1059,11 @@ def main(argv=None):
     ap.add_argument("--graph", choices=["on", "off"], default="on",
                     help="replay each step's launches as a CUDA graph (planning "
                          "stays per step on the host)")
+    ap.add_argument("--copies", choices=["auto", "side", "graph"], default="auto",
+                    help="graph mode: the step's plan / input / output copies on "
+                         "side streams beside the kernel graph (side), or inside "
+                         "one graph per step (graph); auto: graph for steps of at "
+                         "most 64 MiB of KV, side otherwise")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -171,6 +171,27 @@ pkd_status pkd_plan(const pkd_problem *problem, const int32_t *kv_indptr_h,
                     void *int_ws_dev, size_t int_ws_bytes, void *stream);
 
 /*
+ * Copies a plan image (of pkd_plan_host or pkd_plan_shared_prefix_host) from
+ * pinned host memory into int_ws_dev on `stream`, with one small kernel that
+ * reads the host buffer directly (no copy-engine transfer): in a CUDA graph
+ * it chains onto the decode kernel without an engine hand-off ([W] "Plan and
+ * run": a captured run keeps its device addresses while the scheduling data
+ * in them is updated).  The number of words copied is read from the image's
+ * header when the kernel runs, so a captured copy follows whatever plan the
+ * host last wrote into the same buffer; the host must not rewrite the buffer
+ * until the stream has passed the copy.  pinned_image must be page-locked
+ * host memory (cudaHostAlloc / cudaHostRegister), both pointers 16-byte
+ * aligned, and both sizes at least a 64-byte header (else
+ * PKD_ERR_INVALID_ARG / PKD_ERR_UNSUPPORTED / PKD_ERR_WORKSPACE, nothing
+ * launched).  An image that is not a plan, or whose header describes more
+ * words than pinned_image_bytes or int_ws_bytes hold, is not copied beyond
+ * its header, and PKD_DEVICE_BAD_PLAN is set in the device copy's status
+ * word (every kernel then rejects it).
+ */
+pkd_status pkd_copy_plan(const int32_t *pinned_image, size_t pinned_image_bytes,
+                         void *int_ws_dev, size_t int_ws_bytes, void *stream);
+
+/*
  * Decode attention for a planned batch, on `stream`: the decode kernel walks
  * the work list, writing out/lse directly for requests handled by one unit
  * and fp32 partial (output, lse) states to float_ws_dev otherwise; then, if

@@ -7,7 +7,7 @@ kernels.  PyTorch supplies device memory and streams.  If the library is
 missing, every call raises; there is no other implementation to fall back to.
 
 Entry points (same names as the C ABI without the ``pkd_`` prefix):
-``workspace_size``, ``plan_host``, ``plan``, ``run`` (its ``phase`` picks
+``workspace_size``, ``plan_host``, ``plan``, ``copy_plan``, ``run`` (its ``phase`` picks
 ``pkd_run``, ``pkd_run_decode``, ``pkd_run_merge`` or
 ``pkd_run_decode_states``), ``run_static``, ``merge_states``,
 ``check_status``, the shared-prefix calls (``plan_shared_prefix``,
@@ -43,7 +43,7 @@ EXPORTED = ("pkd_abi_version", "pkd_last_error", "pkd_workspace_size",
             "pkd_run_static", "pkd_prefix_workspace_size", "pkd_plan_shared_prefix",
             "pkd_run_shared_prefix", "pkd_append_kv", "pkd_run_shared_prefix_states",
             "pkd_run_cascade", "pkd_run_cascade_merge", "pkd_run_decode_states",
-            "pkd_plan_shared_prefix_host")
+            "pkd_plan_shared_prefix_host", "pkd_copy_plan")
 
 
 class PkdError(RuntimeError):
@@ -128,6 +128,7 @@ def load():
                                                 ctypes.c_int32, ctypes.c_int32,
                                                 ctypes.POINTER(PrefixPlan), i32p,
                                                 ctypes.c_size_t]
+    lib.pkd_copy_plan.argtypes = [i32p, ctypes.c_size_t, vp, ctypes.c_size_t, vp]
     lib.pkd_run_shared_prefix.argtypes = [ctypes.POINTER(PrefixPlan), vp, vp, vp, vp, vp,
                                           ctypes.c_size_t, ctypes.c_float, vp, vp, vp]
     lib.pkd_run_shared_prefix_states.argtypes = [ctypes.POINTER(PrefixPlan), vp, vp, vp,
@@ -202,8 +203,28 @@ def _addr(a):
     return a.ctypes.data
 
 
-def plan_host(problem: Problem, kv_indptr, kv_last_page_len, kv_indices=None):
-    """Host-only planning; returns (Plan, plan image as an int32 array)."""
+def plan_host(problem: Problem, kv_indptr, kv_last_page_len, kv_indices=None, *,
+              image=None):
+    """Host-only planning; returns (Plan, plan image as an int32 array).
+
+    With ``image`` (a host int32 torch tensor, e.g. pinned staging memory,
+    or numpy array) the image is written into it and ``(Plan, image)`` is
+    returned without a copy; otherwise a new array of the image's size.
+    """
+    if image is not None:
+        if problem.num_ctas <= 0:
+            raise ValueError("plan_host needs an explicit num_ctas")
+        if hasattr(image, "data_ptr"):
+            addr, nbytes = image.data_ptr(), image.numel() * image.element_size()
+        else:
+            addr, nbytes = _addr(image), image.nbytes
+        indptr, p_indptr = _host_i32(kv_indptr)
+        last, p_last = _host_i32(kv_last_page_len)
+        idx, p_idx = _host_i32(kv_indices)
+        out = Plan()
+        _check(load().pkd_plan_host(ctypes.byref(problem), p_indptr, p_last, p_idx,
+                                    ctypes.byref(out), addr, nbytes))
+        return out, image
     prob = Problem.from_buffer_copy(problem)
     if prob.num_ctas <= 0:
         raise ValueError("plan_host needs an explicit num_ctas")
@@ -249,6 +270,15 @@ def plan(problem: Problem, kv_indptr, kv_last_page_len, kv_indices=None, *,
                            staging.numel() * staging.element_size(), _ptr(int_ws),
                            int_ws.numel() * int_ws.element_size(), _stream_ptr(stream)))
     return out
+
+
+def copy_plan(image, int_ws, stream=None):
+    """pkd_copy_plan: a plan image in pinned host memory (an int32 torch
+    tensor, e.g. a Workspace's staging buffer) into the device workspace
+    ``int_ws``, by a kernel that reads the host buffer; graph-capturable."""
+    _check(load().pkd_copy_plan(_ptr(image), image.numel() * image.element_size(),
+                                _ptr(int_ws), int_ws.numel() * int_ws.element_size(),
+                                _stream_ptr(stream)))
 
 
 def run(plan_: Plan, q, k_pages, v_pages, kv_indptr, kv_indices, kv_last_page_len,
@@ -387,18 +417,27 @@ def prefix_workspace_size(problem: Problem, max_prefix_pages: int):
     return a.value, b.value, c.value
 
 
-def plan_shared_prefix_host(problem: Problem, prefix_pages, prefix_last_page_len):
-    """Host-only prefix planning; returns (PrefixPlan, image as an int32 array)."""
-    prob = Problem.from_buffer_copy(problem)
-    if prob.num_ctas <= 0:
+def plan_shared_prefix_host(problem: Problem, prefix_pages, prefix_last_page_len, *,
+                            image=None):
+    """Host-only prefix planning; returns (PrefixPlan, image as an int32 array),
+    or ``(PrefixPlan, image)`` written into the given host buffer."""
+    if problem.num_ctas <= 0:
         raise ValueError("plan_shared_prefix_host needs an explicit num_ctas")
     pages, p_pages = _host_i32(prefix_pages)
     n = 0 if prefix_pages is None else int(np.asarray(prefix_pages).size)
-    image = np.zeros(16 + n + 1, dtype=np.int32)
+    given = image is not None
+    if not given:
+        image = np.zeros(16 + n + 1, dtype=np.int32)
+    if hasattr(image, "data_ptr"):
+        addr, nbytes = image.data_ptr(), image.numel() * image.element_size()
+    else:
+        addr, nbytes = _addr(image), image.nbytes
     out = PrefixPlan()
     _check(load().pkd_plan_shared_prefix_host(
-        ctypes.byref(prob), p_pages, n, int(prefix_last_page_len), ctypes.byref(out),
-        _addr(image), image.nbytes))
+        ctypes.byref(problem), p_pages, n, int(prefix_last_page_len), ctypes.byref(out),
+        addr, nbytes))
+    if given:
+        return out, image
     return out, image[: out.int_ws_bytes_used // 4].copy()
 
 

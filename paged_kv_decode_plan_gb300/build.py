@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build", platform.machine())
 LIB_PATH = os.path.join(HERE, "libpkd.so")
 
 SOURCES = ["plan.cpp", "api.cu", "decode.cu", "merge.cu", "prefix.cu", "append.cu",
-           "static_scratch.cu"]
+           "static_scratch.cu", "plan_copy.cu"]
 HEADERS = ["pkd_internal.h", "ptx.cuh", "kernel_common.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
