@@ -34,7 +34,9 @@
 // its fp32 partial slot; in the states-only mode (the cascade's suffix) an
 // unsplit request b also goes to an fp32 slot, num_partials + b.  Every
 // mbarrier wait is bounded; a wait that runs out records PKD_DEVICE_TIMEOUT
-// in the status word and the CTA stops.
+// in the status word and the CTA stops.  (A test hook, read from the
+// environment at launch, can leave out the loader warp or the consumer warps,
+// so that the other role's waits end on the abort path: see launch_decode.)
 //
 // Sources (page title, section):
 //  - "FlashInfer" (aiwiki.ai/wiki/flashinfer), "Block-sparse cache
@@ -51,6 +53,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -71,6 +74,17 @@ constexpr int kStageBudget = 200 * 1024;            // bytes of stages per CTA
 constexpr int kIdPrefetchTiles = 4;
 
 enum Loader : int { kLoaderTma = PKD_LOADER_TMA_TILES, kLoaderBulk = PKD_LOADER_BULK_ROWS };
+
+// Host-side failure injection for tests of the timeout path: one role of the
+// CTA is left out; in its place one thread waits about 100 us and then raises
+// the CTA's abort flag, as a warp whose wait ran out does, so the other role's
+// waits end on the abort path (timeout bit, drain of copies in flight).
+enum Inject : int { kInjectNone = 0, kInjectNoLoader = 1, kInjectNoConsumers = 2 };
+
+__device__ __noinline__ void stall_then_abort(volatile int *abort) {
+  for (int i = 0; i < 100; ++i) __nanosleep(1000);
+  *abort = 1;
+}
 
 // Shared-memory geometry of one stage (K tile, then V tile) for a loader.
 //  * TMA tiled loader: per head [d-half][16 rows][128 B], 16-byte chunks
@@ -109,6 +123,7 @@ struct Params {
   int programmatic;   // launched as a programmatic dependent (host side only)
   int states_only;    // every request's state as fp32: unsplit request b in
                       // slot num_partials + b, nothing into out / lse
+  int inject;         // test hook: kInjectNoLoader / kInjectNoConsumers
   // batch: requests the q / out / lse / page-table buffers hold; a plan may
   // cover fewer (a captured launch replayed with a later, smaller plan)
 };
@@ -637,7 +652,10 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
   __syncthreads();
 
   if (threadIdx.x >= 32 * kConsumerWarps) {
-    if (LOADER == kLoaderTma)
+    if (q.inject == kInjectNoLoader) {
+      // left out (test hook): no copy is issued
+      if ((threadIdx.x & 31) == 0) stall_then_abort(abort);
+    } else if (LOADER == kLoaderTma)
       load_tma<HKV>(q, &map_k, &map_v, units, num_partials, u_begin, u_end, stages,
                     full0, empty0, abort);
     else if (q.page_size < kTile)
@@ -646,6 +664,9 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
     else
       load_bulk<HKV, false>(q, units, num_partials, u_begin, u_end, stages, full0, empty0,
                             abort);
+  } else if (q.inject == kInjectNoConsumers) {
+    // left out (test hook): nothing frees a stage
+    if (threadIdx.x == 0) stall_then_abort(abort);
   } else {
     consume<T, HKV, NG, LOADER>(q, units, num_partials, u_begin, u_end, stages, full0,
                                 empty0, abort);
@@ -861,6 +882,16 @@ int launch_decode(const DecodeArgs &a, void *stream) {
   prm.hnd = a.layout == PKD_LAYOUT_HND;
   prm.programmatic = a.programmatic;
   prm.states_only = a.states_only;
+  // Test hook (host-side failure injection): PKD_TEST_INJECT=no-loader or
+  // no-consumers leaves that role of every CTA out; its stand-in raises the
+  // CTA's abort flag after about 100 us, so the other role's waits give up,
+  // record PKD_DEVICE_TIMEOUT and retire (the loader still waits for every
+  // copy it issued before its CTA exits).  Unset, nothing changes.
+  prm.inject = kInjectNone;
+  if (const char *inj = std::getenv("PKD_TEST_INJECT")) {
+    if (std::strcmp(inj, "no-loader") == 0) prm.inject = kInjectNoLoader;
+    if (std::strcmp(inj, "no-consumers") == 0) prm.inject = kInjectNoConsumers;
+  }
 
   CUtensorMap mk;
   CUtensorMap mv;
