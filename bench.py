@@ -14,7 +14,8 @@ long-context batch (8 x 131072 tokens, Hq 64 / Hkv 8, P 64, bf16, >= 132
 partial states per request + merge), the largest one that fits one GPU.  The
 other four are reported under ``per_config`` in the same line.
 ``--workload NAME`` times one workload alone.  For the cascade workload a step
-plans the suffix table and the shared prefix and runs the shared-prefix
+plans the suffix table (the shared prefix, which does not change between
+decode steps, is planned once per workspace) and runs the shared-prefix
 kernel, the suffix decode and the cascade merge (``--cascade fused``,
 pkd_run_cascade's launches), or the prefix and suffix runs merged by
 merge_states (``--cascade shared``), or the prefix listed in every request's
@@ -308,10 +309,13 @@ class Runner:
                                     num_kv_heads=wl.num_kv_heads, page_size=pt.page_size,
                                     dtype=wl.dtype, num_pages=wl.num_pages,
                                     num_ctas=prefix_ctas, kv_layout=self.layout)
+            # the shared prefix does not change from one decode step to the
+            # next (only the suffixes grow), so each workspace turn plans it
+            # once and reuses the plan; the suffixes are planned every step
             self.prefix = dict(
                 pages=pages, last=int(pt.kv_last_page_len[0]),
                 ws=[pkd.PrefixWorkspace(prob, pages.size, device=device) for _ in range(2)],
-                outs=[self._pair() for _ in range(2)])
+                plans=[None, None], outs=[self._pair() for _ in range(2)])
         self.parts = []
         for n, t in enumerate(self.tables):
             prob = pkd.make_problem(batch=t.batch, num_qo_heads=wl.num_qo_heads,
@@ -403,8 +407,10 @@ class Runner:
                                                  image=part["ws"][i].staging[0])
         if self.prefix is not None:
             pre = self.prefix
-            pre["plan"], _ = self.pkd.plan_shared_prefix_host(
-                pre["problem"], pre["pages"], pre["last"], image=pre["ws"][i].staging)
+            if pre["plans"][i] is None:
+                pre["plans"][i], _ = self.pkd.plan_shared_prefix_host(
+                    pre["problem"], pre["pages"], pre["last"], image=pre["ws"][i].staging)
+            pre["plan"] = pre["plans"][i]
 
     def _step_graph(self, events, inputs, outputs):
         torch = self.torch
@@ -489,8 +495,10 @@ class Runner:
                                               stream=self.copy_stream)
         if self.prefix is not None:
             pre = self.prefix
-            pre["plan"] = pre["ws"][i].plan(pre["pages"], pre["last"],
-                                            stream=self.copy_stream)
+            if pre["plans"][i] is None:
+                pre["plans"][i] = pre["ws"][i].plan(pre["pages"], pre["last"],
+                                                    stream=self.copy_stream)
+            pre["plan"] = pre["plans"][i]
         ready = self.ready_ev[i]
         ready.record(self.copy_stream)
         main.wait_event(ready)
@@ -821,7 +829,7 @@ def measure(args, ranks, device, wl, cpu):
         torch.cuda.synchronize()
         ranks.barrier()
         # end to end through the public API with host buffers
-        e2e = run_e2e(args, runner, device, ranks)
+        e2e = run_e2e(args, runner, device, ranks, elapsed / k)
         clocks.mark(1)
     decode_ms, prefix_ms = runner.read_timings(events)
     agg = aggregate(ranks, runner.kv_bytes(), elapsed, k)
@@ -890,7 +898,7 @@ def _explicit(problem, runner):
     return p
 
 
-def run_e2e(args, runner, device, ranks):
+def run_e2e(args, runner, device, ranks, step_s):
     """Same metric through the public API: every step copies its inputs
     (queries and page table) host-to-device from pinned memory, plans, runs,
     and copies out and lse device-to-host into one of two pinned buffers.
@@ -906,7 +914,12 @@ def run_e2e(args, runner, device, ranks):
     outs_h = [torch.empty(res_bytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
     h2d = in_h.numel()
     d2h = res_bytes
-    steps = max(3, min(args.steps, args.e2e_steps))
+    if args.e2e_steps > 0:
+        steps = args.e2e_steps
+    else:
+        # about 0.2 s of steps (at least K, at most 2000): host jitter on a
+        # loop of a few hundred microseconds would otherwise dominate
+        steps = int(min(2000, max(args.steps, 0.2 / max(step_s, 1e-6))))
 
     def one():
         # each workspace turn reads back into its own pinned buffer
@@ -916,7 +929,8 @@ def run_e2e(args, runner, device, ranks):
         one()
     torch.cuda.synchronize()
     image_bytes = sum(int(p["plan"].int_ws_bytes_used) for p in runner.parts)
-    if runner.prefix is not None:
+    if runner.prefix is not None and runner.use_graph and runner.copies == "graph":
+        # the step's graph copies the (unchanged) prefix image too
         image_bytes += int(runner.prefix["plan"].int_ws_bytes_used)
 
     ranks.barrier()
@@ -1037,7 +1051,9 @@ def main(argv=None):
                     help="all (default): every workload timed in one run, the "
                          "long-context batch as the headline line and the others "
                          "under per_config")
-    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="steps of the end-to-end loop (0: about 0.2 s of steps, "
+                         "at least --steps, at most 2000)")
     ap.add_argument("--layout", choices=["nhd", "hnd"], default="nhd",
                     help="page tensor layout (the same values either way)")
     ap.add_argument("--cascade-split", choices=["on", "off"], default="on",
