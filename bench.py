@@ -689,7 +689,9 @@ def workload_config(wl):
             "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
             "page_size": wl.page_size, "kv_bytes_per_step": kv,
             "l2": ("inputs larger than L2 (KV %.0f MB vs 129 MB), no flush" % (kv / 1e6))
-            if kv > 2 * L2_BYTES else "KV fits in L2: warm-L2 number",
+            if kv > 2 * L2_BYTES else
+            ("KV (%.1f MB) fits in L2: L2 flushed before every timed step; "
+             "e2e and warm_us_per_batch warm" % (kv / 1e6)),
             "parallelism": "replicas (weak scaling, no collective)"}
 
 
@@ -737,9 +739,11 @@ def config_summary(line):
     keys = ("us_per_batch", "value", "unit", "ms_per_step", "steps", "warmup",
             "decode_us", "prefix_us", "host_enqueue_us_per_step", "total_gbs",
             "plan_host_us", "num_units", "num_split_requests", "launch", "copies",
+            "warm_us_per_batch",
             "gpu_launches", "dtype", "clocks")
     out = {"workload": line["config"]["workload"],
-           "kv_bytes_per_step": line["config"]["kv_bytes_per_step"]}
+           "kv_bytes_per_step": line["config"]["kv_bytes_per_step"],
+           "l2": line["config"]["l2"]}
     out.update({k: line[k] for k in keys if k in line})
     peak_key = [k for k in line if k.startswith("hbm_frac_of_")][0]
     out["step_" + peak_key] = line[peak_key]
@@ -803,6 +807,12 @@ def measure(args, ranks, device, wl, cpu):
     events = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
               for _ in range(k)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # a batch whose KV fits in L2 is timed cold: a write of twice L2's size
+    # before every timed step, the steps timed one by one (the warm figure is
+    # reported beside it); larger batches stream more than L2 every step
+    small = runner.kv_bytes() <= 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if small else None
+    warm_s = None
     with ClockSampler(uuid) as clocks:
         # the W warm-up steps run right before the timed region (the clock
         # sampler's start-up pause would otherwise sit between them)
@@ -812,19 +822,41 @@ def measure(args, ranks, device, wl, cpu):
         # pass 1: the whole step, start and end events only
         ranks.barrier()
         torch.cuda.synchronize()
-        start.record(stream)
-        h0 = time.perf_counter()
-        for _ in range(k):
-            runner.step()
-        host_s = time.perf_counter() - h0
-        end.record(stream)
-        torch.cuda.synchronize()
+        if small:
+            step_ev = [(torch.cuda.Event(enable_timing=True),
+                        torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+            host_s = 0.0
+            for i in range(k):
+                flush_buf.fill_(i & 0xFF)
+                step_ev[i][0].record(stream)
+                h0 = time.perf_counter()
+                runner.step()
+                host_s += time.perf_counter() - h0
+                step_ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            elapsed = sum(a.elapsed_time(b) for a, b in step_ev) / 1e3
+            start.record(stream)
+            for _ in range(k):
+                runner.step()
+            end.record(stream)
+            torch.cuda.synchronize()
+            warm_s = start.elapsed_time(end) / 1e3
+        else:
+            start.record(stream)
+            h0 = time.perf_counter()
+            for _ in range(k):
+                runner.step()
+            host_s = time.perf_counter() - h0
+            end.record(stream)
+            torch.cuda.synchronize()
+            elapsed = start.elapsed_time(end) / 1e3
         ranks.barrier()
-        elapsed = start.elapsed_time(end) / 1e3
         # pass 2: the same steps with events around every decode launch
         ranks.barrier()
         torch.cuda.synchronize()
         for i in range(k):
+            if small:
+                flush_buf.fill_(i & 0xFF)
             runner.step(events[i])
         torch.cuda.synchronize()
         ranks.barrier()
@@ -865,10 +897,15 @@ def measure(args, ranks, device, wl, cpu):
         "launch": ("graph" if runner.use_graph else "eager"),
         "copies": runner.copies,
         "timing": "W warm-up steps right before pass 1; pass 1 (value, ms_per_step): K "
-                  "steps between two events; pass 2 (decode_us, roofline): the same K "
-                  "steps with events around each decode launch" +
+                  + ("steps, each after an L2 flush (a %d MB write) and timed alone "
+                     "between two events (warm_us_per_batch: the same K steps back "
+                     "to back without flushes)" % (2 * L2_BYTES >> 20) if small else
+                     "steps between two events")
+                  + "; pass 2 (decode_us, roofline): the same K steps with events "
+                  "around each decode launch" +
                   (" (inside the replayed graph, one step at a time)"
                    if runner.use_graph else ""),
+        "warm_us_per_batch": (round(warm_s / k * 1e6, 2) if warm_s is not None else None),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel",
                      "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
