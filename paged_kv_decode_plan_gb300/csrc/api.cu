@@ -516,7 +516,6 @@ pkd_status pkd_run_cascade_merge(const pkd_plan_t *plan, void *int_ws_dev,
   m.lse = lse;
   m.num_qo_heads = p.num_qo_heads;
   m.dtype = p.dtype;
-  m.grid = 4 * p.num_ctas;  // upper bound on CTAs; rows loop inside
   m.batch = p.batch;
   m.chunks = prefix_plan->chunks;
   m.max_partials = bounds.max_partials;

@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(kMergeThreads)
 // (the decode kernel ran in its states-only mode): the request's partial
 // slots if the suffix plan split it, else slot num_partials + b.  The final
 // state is rounded to the output type once.  The suffix plan lists its split
-// requests in increasing order; a warp finds b among them 32 at a time with a
-// ballot.
+// requests in increasing order; a warp finds b among them 128 at a time (all
+// loads in flight) with ballots, before it waits for the decode grid.
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads)
     cascade_merge_kernel(const int32_t *image, const float *partials,
@@ -143,35 +143,51 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int32_t *merge_req = image + o.merge_req;
   const long long slot_floats = partial_slot_floats(hq, kHeadDim);
   const long long rows = static_cast<long long>(batch) * hq;
-  // a programmatic dependent of the decode kernel, whose threads wait for the
-  // prefix kernel before exiting: once the decode kernel is complete, both
-  // kernels' states are in place
-  ptx::wait_primary_grid();
-  for (long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       row < rows; row += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
-    const int b = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
+  // (suffix slot range) of request b: its partial slots if the suffix plan
+  // split it, else slot num_partials + b.  The split requests are listed in
+  // increasing order; 128 entries are read per round, all in flight at once.
+  auto describe = [&](int b, int &s0, int &s1) {
     int split = -1;
-    for (int base = 0; base < num_split; base += 32) {
-      const int r = base + lane < num_split ? merge_req[base + lane] : INT_MAX;
-      const unsigned hit = __ballot_sync(0xffffffffu, r == b);
-      if (hit) {
-        split = base + __ffs(hit) - 1;
-        break;
+    for (int base = 0; base < num_split && split < 0; base += 128) {
+      int r[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int idx = base + 32 * k + lane;
+        r[k] = idx < num_split ? merge_req[idx] : INT_MAX;
       }
-      if (__shfl_sync(0xffffffffu, r, 31) > b) break;  // past b: not split
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const unsigned hit = __ballot_sync(0xffffffffu, r[k] == b);
+        if (hit && split < 0) split = base + 32 * k + __ffs(hit) - 1;
+      }
+      if (__shfl_sync(0xffffffffu, r[3], 31) > b) break;  // past b: not split
     }
+    if (split >= 0) {
+      s0 = max(0, merge_indptr[split]);
+      s1 = min(num_partials, merge_indptr[split + 1]);
+    } else {
+      s0 = num_partials + b;
+      s1 = s0 + 1;
+    }
+  };
+  // The plan images were in place before the kernels of this step started,
+  // so the first row is described before the wait; the states are read only
+  // after it.  This kernel is a programmatic dependent of the decode kernel,
+  // whose threads wait for the prefix kernel before exiting: once the decode
+  // kernel is complete, both kernels' states are in place.
+  long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  int s0 = 0, s1 = 0;
+  if (row < rows) describe(static_cast<int>(row / hq), s0, s1);
+  ptx::wait_primary_grid();
+  for (bool first = true; row < rows;
+       row += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5, first = false) {
+    const int b = static_cast<int>(row / hq), h = static_cast<int>(row % hq);
+    if (!first) describe(b, s0, s1);
     float m = -INFINITY, ws = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     fold_states<8>(prefix_partials, slot_floats, hq, h, b * chunks, (b + 1) * chunks, 1,
                    lane, m, ws, acc);
-    if (split >= 0) {
-      const int s0 = max(0, merge_indptr[split]);
-      const int s1 = min(num_partials, merge_indptr[split + 1]);
-      fold_states(partials, slot_floats, hq, h, s0, s1, 1, lane, m, ws, acc);
-    } else {
-      fold_states(partials, slot_floats, hq, h, num_partials + b, num_partials + b + 1, 1,
-                  lane, m, ws, acc);
-    }
+    fold_states(partials, slot_floats, hq, h, s0, s1, 1, lane, m, ws, acc);
     write_state<T>(out, lse, b, hq, h, lane, m, ws, acc);
   }
 }
@@ -423,12 +439,15 @@ int launch_merge_uniform(const float *partials, void *out, float *lse, int batch
 int launch_cascade_merge(const CascadeMergeArgs &a, void *stream) {
   const long long rows = static_cast<long long>(a.batch) * a.num_qo_heads;
   if (rows == 0) return cudaSuccess;
+  // one warp per row: every row is described before the wait on the decode
+  // grid, and only its state loads come after it
   const long long want = (rows + kMergeWarps - 1) / kMergeWarps;
+  const long long grid = want < 65535 ? want : 65535;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(want < a.grid ? want : a.grid));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;

@@ -150,7 +150,7 @@ struct CascadeMergeArgs {
   const float *prefix_partials;  // prefix chunk states
   void *out;
   float *lse;
-  int num_qo_heads, dtype, grid;
+  int num_qo_heads, dtype;
   int batch, chunks;             // of the prefix plan (the suffix image must agree)
   int max_partials, image_words; // bounds for the suffix image
 };
