@@ -355,6 +355,10 @@ class Runner:
         self.launches_per_step = 0
         self.use_graph = graph
         self.copies = copies if graph else "side"
+        # kernels of a step besides those of _launch: the plan-image copies
+        # (pkd_copy_plan) of the one-graph schedule
+        self.extra_launches = (len(self.tables) + (1 if self.shared else 0)
+                               if self.copies == "graph" else 0)
         self.eager_steps = 0
         self.graphs = {}
         # timing events inside a graph must be real event-record nodes
@@ -460,8 +464,6 @@ class Runner:
                 outputs.copy_(self.result_turn(i)[2], non_blocking=True)
         torch.cuda.synchronize()
         self.graphs[(i, timed, inputs is not None)] = g
-        # graph launches of this step: the kernels of _launch (copies are not
-        # counted as kernels)
 
     def _capture_kernels(self, i, timed):
         """Turn i's kernel launches as one graph (valid for every later plan
@@ -917,7 +919,7 @@ def measure(args, ranks, device, wl, cpu):
                                  and args.batch is None else None),
                      "algorithmic_bytes_per_launch": runner.decode_kv_bytes()},
         "e2e": e2e,
-        "gpu_launches": runner.launches_per_step * k,
+        "gpu_launches": (runner.launches_per_step + runner.extra_launches) * k,
         "clocks": clocks.summary(),
     }
     if cpu and ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:

@@ -84,6 +84,12 @@ typedef enum {
 #define PKD_DEVICE_BAD_LENGTH 2u  /* a plan unit runs past the request */
 #define PKD_DEVICE_BAD_PLAN 4u    /* workspace does not hold a plan image */
 #define PKD_DEVICE_TIMEOUT 8u     /* a bounded pipeline wait ran out */
+/* Test hook: with the environment variable PKD_TEST_INJECT set to "no-loader"
+ * or "no-consumers" when a decode kernel is launched, that role of every CTA
+ * is left out and, after about 100 us, the CTA's abort flag is raised, so the
+ * other role's waits give up and record PKD_DEVICE_TIMEOUT (a host-side
+ * failure injection for tests of the timeout path; the results of such a
+ * launch are meaningless).  Unset in normal use. */
 
 /* Problem geometry and planning knobs. */
 typedef struct {
