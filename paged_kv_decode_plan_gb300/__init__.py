@@ -203,6 +203,16 @@ def _addr(a):
     return a.ctypes.data
 
 
+def _require_host(image):
+    """A host planner writes the image through a CPU pointer: refuse device
+    tensors and anything that is not int32."""
+    if getattr(image, "is_cuda", False):
+        raise ValueError("the plan image buffer must be host memory")
+    dt = getattr(image, "dtype", None)
+    if dt is not None and str(dt) not in ("torch.int32", "int32"):
+        raise ValueError("the plan image buffer must be int32")
+
+
 def plan_host(problem: Problem, kv_indptr, kv_last_page_len, kv_indices=None, *,
               image=None):
     """Host-only planning; returns (Plan, plan image as an int32 array).
@@ -214,6 +224,7 @@ def plan_host(problem: Problem, kv_indptr, kv_last_page_len, kv_indices=None, *,
     if image is not None:
         if problem.num_ctas <= 0:
             raise ValueError("plan_host needs an explicit num_ctas")
+        _require_host(image)
         if hasattr(image, "data_ptr"):
             addr, nbytes = image.data_ptr(), image.numel() * image.element_size()
         else:
@@ -276,6 +287,7 @@ def copy_plan(image, int_ws, stream=None):
     """pkd_copy_plan: a plan image in pinned host memory (an int32 torch
     tensor, e.g. a Workspace's staging buffer) into the device workspace
     ``int_ws``, by a kernel that reads the host buffer; graph-capturable."""
+    _require_host(image)
     _check(load().pkd_copy_plan(_ptr(image), image.numel() * image.element_size(),
                                 _ptr(int_ws), int_ws.numel() * int_ws.element_size(),
                                 _stream_ptr(stream)))
@@ -426,7 +438,9 @@ def plan_shared_prefix_host(problem: Problem, prefix_pages, prefix_last_page_len
     pages, p_pages = _host_i32(prefix_pages)
     n = 0 if prefix_pages is None else int(np.asarray(prefix_pages).size)
     given = image is not None
-    if not given:
+    if given:
+        _require_host(image)
+    else:
         image = np.zeros(16 + n + 1, dtype=np.int32)
     if hasattr(image, "data_ptr"):
         addr, nbytes = image.data_ptr(), image.numel() * image.element_size()

@@ -140,3 +140,45 @@ def test_cascade_checks_the_suffix_states_workspace():
     assert lib.pkd_run_cascade_merge(ctypes.byref(plan), FAKE, FAKE, _states_bytes(plan) - 1,
                                      ctypes.byref(pp), FAKE, FAKE, 1 << 30, FAKE, FAKE,
                                      None) == WORKSPACE
+
+
+def test_plan_host_into_caller_buffer_and_guards():
+    """plan_host / plan_shared_prefix_host write into a given host int32
+    buffer (returned as is, the same image as a fresh plan) and refuse device
+    or non-int32 buffers before calling the library."""
+    import numpy as np
+    import paged_kv_decode_plan_gb300 as pkd
+    prob = pkd.make_problem(batch=2, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                            dtype="f16", num_pages=64, num_ctas=8)
+    indptr = np.array([0, 3, 5], np.int32)
+    last = np.array([16, 7], np.int32)
+    buf = np.full(4096, -1, np.int32)
+    plan, img = pkd.plan_host(prob, indptr, last, image=buf)
+    assert img is buf
+    _, fresh = pkd.plan_host(prob, indptr, last)
+    n = plan.int_ws_bytes_used // 4
+    assert np.array_equal(buf[:n], fresh)
+
+    class FakeDevice:
+        is_cuda = True
+        dtype = "int32"
+    for bad in (np.zeros(1024, np.int64), FakeDevice()):
+        try:
+            pkd.plan_host(prob, indptr, last, image=bad)
+        except ValueError:
+            pass
+        else:
+            raise AssertionError("accepted %r" % (bad,))
+    pprob = pkd.make_problem(batch=2, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                             dtype="f16", num_pages=64, num_ctas=16)
+    pbuf = np.zeros(64, np.int32)
+    pplan, pimg = pkd.plan_shared_prefix_host(pprob, np.array([4, 9, 2], np.int32), 5,
+                                              image=pbuf)
+    assert pimg is pbuf and pplan.prefix_len == 37
+    try:
+        pkd.plan_shared_prefix_host(pprob, np.array([4, 9, 2], np.int32), 5,
+                                    image=FakeDevice())
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("accepted a device buffer")
