@@ -78,3 +78,31 @@ def test_bench_runner_large_workloads_sampled(name):
     for _ in range(5):
         runner.step()
     print(name, _check(runner, wl, _sample(wl, 48, 4)))
+
+
+@pytest.mark.parametrize("layout,loader", [("hnd", 0), ("nhd", 1), ("nhd", 2), ("hnd", 2)])
+def test_bench_runner_layouts_and_loaders(layout, loader):
+    """batch-64 through the Runner with HND pages (the bench transposes the
+    same values) and each K/V loader."""
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device")
+    wl = workloads.batch64()
+    runner = bench.Runner(wl, torch.device("cuda", 0), graph=True, copies="side",
+                          layout=layout, kv_loader=loader)
+    for _ in range(6):
+        runner.step()
+    _check(runner, wl)
+
+
+@pytest.mark.parametrize("cascade", ["shared", "per-request"])
+def test_bench_runner_cascade_modes(cascade):
+    """The composed cascade (prefix run + suffix run + merge_states) and the
+    prefix listed in every request's table."""
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device")
+    wl = workloads.cascade()
+    runner = bench.Runner(wl, torch.device("cuda", 0), graph=True, copies="side",
+                          cascade=cascade)
+    for _ in range(6):
+        runner.step()
+    _check(runner, wl, _sample(wl, 200, 5))
