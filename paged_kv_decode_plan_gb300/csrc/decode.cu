@@ -145,8 +145,9 @@ __device__ Unit read_unit(const Params &p, const int32_t *units, int u,
   r.t1 = ptx::ldg_keep(w + 2, keep);
   r.slot = ptx::ldg_keep(w + 3, keep);
   r.pbase = 0;
+  // a unit starts on a tile boundary (the host planner never emits another)
   if (r.req < 0 || r.req >= p.batch || r.slot < -1 || r.slot >= num_partials ||
-      r.t0 < 0 || r.t1 < r.t0) {
+      r.t0 < 0 || r.t1 < r.t0 || r.t0 % kTile != 0) {
     if (threadIdx.x == 0) flag(p.image, PKD_DEVICE_BAD_PLAN);
     r.req = -1;
     r.t0 = r.t1 = 0;
