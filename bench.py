@@ -739,7 +739,8 @@ def run_ours(args, ranks):
 def config_summary(line):
     """The figures of one workload's line that per_config reports."""
     keys = ("us_per_batch", "value", "unit", "ms_per_step", "steps", "warmup",
-            "decode_us", "prefix_us", "host_enqueue_us_per_step", "total_gbs",
+            "decode_us", "prefix_us", "host_enqueue_us_per_step", "host_cpu_us_per_step",
+            "total_gbs",
             "plan_host_us", "num_units", "num_split_requests", "launch", "copies",
             "warm_us_per_batch",
             "gpu_launches", "dtype", "clocks")
@@ -827,13 +828,14 @@ def measure(args, ranks, device, wl, cpu):
         if small:
             step_ev = [(torch.cuda.Event(enable_timing=True),
                         torch.cuda.Event(enable_timing=True)) for _ in range(k)]
-            host_s = 0.0
+            host_s = host_cpu_s = 0.0
             for i in range(k):
                 flush_buf.fill_(i & 0xFF)
                 step_ev[i][0].record(stream)
-                h0 = time.perf_counter()
+                h0, c0 = time.perf_counter(), time.thread_time()
                 runner.step()
                 host_s += time.perf_counter() - h0
+                host_cpu_s += time.thread_time() - c0
                 step_ev[i][1].record(stream)
             torch.cuda.synchronize()
             elapsed = sum(a.elapsed_time(b) for a, b in step_ev) / 1e3
@@ -845,10 +847,11 @@ def measure(args, ranks, device, wl, cpu):
             warm_s = start.elapsed_time(end) / 1e3
         else:
             start.record(stream)
-            h0 = time.perf_counter()
+            h0, c0 = time.perf_counter(), time.thread_time()
             for _ in range(k):
                 runner.step()
             host_s = time.perf_counter() - h0
+            host_cpu_s = time.thread_time() - c0
             end.record(stream)
             torch.cuda.synchronize()
             elapsed = start.elapsed_time(end) / 1e3
@@ -887,6 +890,10 @@ def measure(args, ranks, device, wl, cpu):
         # host time to enqueue one step in pass 1 (plan + copies + launches);
         # above us_per_batch the step is host-bound
         "host_enqueue_us_per_step": round(host_s / k * 1e6, 2),
+        # CPU time of the enqueuing thread in the same loop (waits for the
+        # device spin, so they count too); far below the wall time above,
+        # the thread was descheduled
+        "host_cpu_us_per_step": round(host_cpu_s / k * 1e6, 2),
         "plan_host_us": round(statistics.median(plan_times) * 1e6, 1),
         "num_units": runner.parts[0]["plan"].num_units,
         "num_split_requests": runner.parts[0]["plan"].num_split_requests,
