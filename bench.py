@@ -47,6 +47,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("paged decode attention µs/batch and KV GB/s as fraction of "
           "GB300 HBM peak")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 GRAPH_COPIES_MAX_KV = 64 * 1024 * 1024
 DESCRIPTIONS = {
@@ -128,6 +129,16 @@ def load_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def load_tensor_peak():
+    """Measured dense bf16 burst TFLOP/s (f16 has the same nominal rate)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_hash() -> str:
@@ -758,6 +769,32 @@ def config_summary(line):
     if line.get("cascade"):
         out["cascade"] = line["cascade"]
         out["cascade_ctas"] = line["cascade_ctas"]
+    if line.get("prefix_roofline"):
+        out["prefix_roofline"] = line["prefix_roofline"]
+    return out
+
+
+def prefix_roofline(runner, prefix_ms):
+    """Tensor roofline of the shared-prefix kernel: 4 * B * Hq * L * D flops
+    (Q K^T and P V) per launch over its mean launch time."""
+    wl = runner.wl
+    pt = wl.extra_tables["prefix"]
+    n_pages = int(pt.kv_indptr[1])
+    length = (n_pages - 1) * pt.page_size + int(pt.kv_last_page_len[0])
+    flops = 4.0 * pt.batch * wl.num_qo_heads * length * wl.head_dim
+    achieved = flops / (prefix_ms * 1e-3) / 1e12
+    peak, kind = load_tensor_peak()
+    ctas, _ = runner.cascade_ctas
+    sms = runner.torch.cuda.get_device_properties(runner.device).multi_processor_count
+    out = {"bound": "tensor", "kernel": "shared_prefix_kernel",
+           "achieved": round(achieved, 1), "peak": peak,
+           "peak_kind": kind + " bf16 burst (f16 has the same nominal rate)",
+           "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+           "algorithmic_flops_per_launch": flops}
+    if ctas:
+        # the kernel runs on `ctas` SMs beside the suffix decode
+        out["ctas"] = ctas
+        out["frac_of_its_sms"] = round(achieved / (peak * ctas / sms), 4)
     return out
 
 
@@ -903,6 +940,8 @@ def measure(args, ranks, device, wl, cpu):
         "cascade_ctas": (list(runner.cascade_ctas) if runner.fused else None),
         "prefix_us": (round(statistics.fmean(prefix_ms) * 1e3, 2)
                       if prefix_ms else None),
+        "prefix_roofline": (prefix_roofline(runner, statistics.fmean(prefix_ms))
+                            if prefix_ms else None),
         "launch": ("graph" if runner.use_graph else "eager"),
         "copies": runner.copies,
         "timing": "W warm-up steps right before pass 1; pass 1 (value, ms_per_step): K "
