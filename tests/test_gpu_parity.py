@@ -259,6 +259,32 @@ def test_device_checks_flag_and_skip():
     assert pkd.check_status(ws.int_ws) == 0
 
 
+def test_unit_off_a_tile_boundary_is_refused():
+    # a plan unit must start on a tile boundary: one planted in the device copy
+    # of the image (t0 = 1) is flagged and skipped, the other requests are
+    # untouched
+    wl = workloads.make_paged("misaligned", [100, 500, 900, 33], num_qo_heads=32,
+                              num_kv_heads=8, page_size=16, dtype="f16", seed=8)
+    dev = gh.DeviceBatch(wl)
+    prob = pkd.make_problem(batch=4, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                            dtype="f16", num_pages=wl.num_pages, num_ctas=4)
+    ws = pkd.Workspace(prob)
+    plan = ws.plan(wl.table.kv_indptr, wl.table.kv_last_page_len, wl.table.kv_indices)
+    img = ws.int_ws[: plan.int_ws_bytes_used].cpu().numpy().view(np.int32)
+    num_ctas = int(img[3])
+    units = 16 + num_ctas + 1
+    first = [u for u in range(int(img[4])) if img[units + 4 * u] == 0][0]
+    assert img[units + 4 * first + 1] == 0 and img[units + 4 * first + 3] == -1
+    ws.int_ws.view(torch.int32)[units + 4 * first + 1] = 1
+    indptr, indices, last = gh.device_table(wl.table)
+    out, lse = ws.run(plan, dev.q, dev.k, dev.v, indptr, indices, last, wl.sm_scale)
+    torch.cuda.synchronize()
+    assert pkd.check_status(ws.int_ws) & pkd.DEVICE_BAD_PLAN
+    rows = np.arange(wl.num_qo_heads, 4 * wl.num_qo_heads, dtype=np.int64)
+    ref_out, ref_lse = gh.oracle_ref(wl, rows=rows)
+    gh.compare(out, lse, ref_out, ref_lse, wl.dtype, rows=rows)
+
+
 def test_run_rejects_bad_arguments():
     wl = workloads.make_paged("args", [400], num_qo_heads=8, num_kv_heads=8,
                               page_size=16, dtype="f16", seed=6)
