@@ -51,7 +51,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -675,24 +674,17 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + Geometry<HKV, LOADER>::
   ptx::wait_primary_grid();
 }
 
-constexpr int kMaxDevices = 64;
-
 template <typename T, int HKV, int NG, int LOADER>
 int launch_typed(const Params &prm, const CUtensorMap &mk, const CUtensorMap &mv,
                  void *stream) {
   using G = Geometry<HKV, LOADER>;
   auto kernel = decode_kernel<T, HKV, NG, LOADER>;
   const int smem = G::kSmemBytes;
-  // the dynamic shared-memory limit is raised once per device
-  static std::atomic<bool> raised[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // the dynamic shared-memory limit is raised on every launch (about 0.2 us
+  // of host time on GB300): a flag kept per process would go stale after a
+  // cudaDeviceReset, which resets the kernel's attributes
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices || !raised[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) raised[dev].store(true, std::memory_order_release);
-  }
   if (prm.programmatic) {
     // may start while the kernel before it on the stream still runs
     cudaLaunchAttribute attr[1];
