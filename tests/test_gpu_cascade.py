@@ -229,7 +229,7 @@ def _random_case(i):
                 min_chunks=int(rng.choice([1, 2, 4])), seed=300 + i)
 
 
-@pytest.mark.parametrize("i", range(16))
+@pytest.mark.parametrize("i", range(64))
 def test_cascade_random_cases(i):
     c = _random_case(i)
     wl, pre_pages, pre_last, prefix, suffix = _case(c["batch"], c["hq"], c["hkv"], c["page"],

@@ -22,7 +22,7 @@ from tests import gpu_helpers as gh
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 48
+N_CASES = 240
 MAX_TOKENS = 24000      # keeps the oracle at well under a second per case
 
 
