@@ -52,13 +52,16 @@ def test_bench_runner_matches_oracle(name, copies):
     _check(runner, wl, rows)
 
 
-def test_bench_runner_end_to_end_step_matches_oracle():
+@pytest.mark.parametrize("name,copies", [("single", "graph"), ("single", "side"),
+                                         ("cascade", "side")])
+def test_bench_runner_end_to_end_step_matches_oracle(name, copies):
     """A step with host inputs copied in and the result read back into pinned
-    memory (the e2e loop's step), one graph per step."""
+    memory (the e2e loop's step): one graph per step, or the copies on their
+    own streams beside the kernels' graph."""
     if not torch.cuda.is_available():
         pytest.fail("no CUDA device")
-    wl = workloads.single()
-    runner = bench.Runner(wl, torch.device("cuda", 0), graph=True, copies="graph")
+    wl = getattr(workloads, name)()
+    runner = bench.Runner(wl, torch.device("cuda", 0), graph=True, copies=copies)
     in_h = runner.host_inputs()
     res_bytes = runner.result()[2].numel()
     outs = [torch.empty(res_bytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
@@ -66,7 +69,7 @@ def test_bench_runner_end_to_end_step_matches_oracle():
         runner.step(inputs=in_h, outputs=outs[runner.turn])
     torch.cuda.synchronize()
     assert torch.equal(outs[runner.last_turn], runner.result()[2].cpu())
-    _check(runner, wl)
+    _check(runner, wl, None if name == "single" else _sample(wl, 100, 6))
 
 
 @pytest.mark.parametrize("name", ["longtail", "longctx"])
