@@ -735,6 +735,16 @@ def run_ours(args, ranks):
     import torch
     torch.cuda.set_device(ranks.local)
     device = torch.device("cuda", ranks.local)
+    if args.workload == "append":
+        ap = measure_append(args, device, cpu=ranks.rank == 0)
+        return {"metric": "page append: K/V bytes read + written per second", "value":
+                ap["bulk"]["value"], "unit": "GB/s", "n_gpus": ranks.world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ap["bulk"]["us"] / 1e3, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f16", "data": "synthetic (seeded N(0,1))",
+                "config": {"workload": APPEND_DESCRIPTION, "name": "append"},
+                **{k_: ap[k_] for k_ in ("bulk", "decode_step", "roofline", "gpu_launches")},
+                **({"cpu_baseline": ap["cpu_baseline"]} if "cpu_baseline" in ap else {})}
     names = ALL_ORDER if args.workload == "all" else [args.workload]
     lines = {}
     for name in names:
@@ -748,7 +758,162 @@ def run_ours(args, ranks):
         line["per_config"] = {n: config_summary(lines[n]) for n in names[:-1]}
         line["config"]["per_config"] = ("the other four workloads, each timed in this "
                                         "run with the same steps and warm-up")
+        # the page append step (new tokens' K/V into their pages), beside the
+        # decode path it feeds
+        line["page_append"] = measure_append(args, device, cpu=ranks.rank == 0)
     return line
+
+
+APPEND_DESCRIPTION = ("page append on the batch-64 page pool (Hkv 8, D 128, P 16, fp16): "
+                      "every token of the 64 requests rewritten (bulk), and one new "
+                      "token per request (a decode step's append)")
+
+
+def measure_append(args, device, cpu=True):
+    """The page-append step on the batch-64 page pool, HBM-bound (a copy):
+    a bulk append that rewrites every token of every request (new K/V rows
+    read, page slots written) timed over the run's steps, and a decode
+    step's append (one token per request, at its last position), each launch
+    between two events inside a replayed graph.  Sampled rows are checked against the new rows; the
+    oracle (oracle/append_ref.py) is timed on a compact pool of the first
+    requests."""
+    import torch
+    import paged_kv_decode_plan_gb300 as pkd
+    from paged_kv_decode_plan_gb300 import workloads
+    wl = workloads.batch64()
+    t = wl.table
+    hkv, d = wl.num_kv_heads, wl.head_dim
+    row_bytes = hkv * d * 2
+    lengths = t.lengths()
+    k = wl.k_pages.to(device)
+    v = wl.v_pages.to(device)
+    tab = [torch.from_numpy(a).to(device) for a in (t.kv_indptr, t.kv_indices,
+                                                    t.kv_last_page_len)]
+    prob = pkd.make_problem(batch=t.batch, num_qo_heads=wl.num_qo_heads, num_kv_heads=hkv,
+                            page_size=t.page_size, dtype=wl.dtype, num_pages=wl.num_pages)
+    bi = np.repeat(np.arange(t.batch, dtype=np.int32), lengths)
+    pos = np.concatenate([np.arange(n, dtype=np.int32) for n in lengths])
+    n = int(bi.size)
+    gen = torch.Generator(device=device).manual_seed(4242)
+    kn = torch.randn(n, hkv, d, generator=gen, device=device).to(k.dtype)
+    vn = torch.randn(n, hkv, d, generator=gen, device=device).to(k.dtype)
+    bi_d, pos_d = torch.from_numpy(bi).to(device), torch.from_numpy(pos).to(device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def bulk():
+        pkd.append_kv(prob, kn, vn, bi_d, pos_d, k, v, *tab, status=status)
+
+    for _ in range(args.warmup):
+        bulk()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        bulk()
+    end.record()
+    torch.cuda.synchronize()
+    bulk_s = start.elapsed_time(end) / 1e3 / args.steps
+    if int(status.item()) != 0:
+        raise RuntimeError("append status word %d" % int(status.item()))
+    # sampled rows: page kv_indices[indptr[b] + pos // P], slot pos % P
+    rng = np.random.default_rng(7)
+    for i in rng.choice(n, size=32, replace=False).tolist():
+        b, p_ = int(bi[i]), int(pos[i])
+        page = int(t.kv_indices[int(t.kv_indptr[b]) + p_ // t.page_size])
+        slot = p_ % t.page_size
+        if not (torch.equal(k[page, slot], kn[i]) and torch.equal(v[page, slot], vn[i])):
+            raise RuntimeError("appended row differs from the new row")
+    moved = 2 * n * row_bytes * 2       # K and V rows, read once and written once
+    peak, peak_kind = load_peak()
+    achieved = moved / bulk_s / 1e9
+
+    # a decode step's append: one token per request, at its last position
+    live = np.nonzero(lengths > 0)[0].astype(np.int32)
+    bi1 = torch.from_numpy(live).to(device)
+    pos1 = torch.from_numpy((lengths[live] - 1).astype(np.int32)).to(device)
+    kn1, vn1 = kn[: live.size].contiguous(), vn[: live.size].contiguous()
+    # replayed as a graph with its events inside (event-record nodes:
+    # "external" events), so that the interval holds the device's work and
+    # not the host's submission of an eager launch
+    try:
+        e0, e1 = (torch.cuda.Event(enable_timing=True, external=True) for _ in range(2))
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=torch.cuda.Stream(device)):
+            e0.record()
+            pkd.append_kv(prob, kn1, vn1, bi1, pos1, k, v, *tab, status=status)
+            e1.record()
+        step_timing = "events inside a replayed graph"
+    except TypeError:
+        e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        graph = None
+        step_timing = "events around an eager launch (host submission included)"
+    step_ts = []
+    for it in range(args.warmup + args.steps):
+        if graph is not None:
+            graph.replay()
+        else:
+            e0.record()
+            pkd.append_kv(prob, kn1, vn1, bi1, pos1, k, v, *tab, status=status)
+            e1.record()
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            step_ts.append(e0.elapsed_time(e1) * 1e3)
+    if int(status.item()) != 0:
+        raise RuntimeError("append status word %d" % int(status.item()))
+    out = {"workload": APPEND_DESCRIPTION,
+           "bulk": {"tokens": n, "us": round(bulk_s * 1e6, 2),
+                    "bytes_per_launch": moved, "value": round(achieved, 1), "unit": "GB/s"},
+           "decode_step": {"tokens": int(live.size),
+                           "us_median": round(statistics.median(step_ts), 2),
+                           "timing": step_timing},
+           "roofline": {"bound": "hbm", "kernel": "append_kernel",
+                        "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                        "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                        "algorithmic_bytes_per_launch": moved},
+           # launches inside the two timed loops
+           "gpu_launches": 2 * args.steps}
+    if cpu:
+        out["cpu_baseline"] = append_cpu_baseline(wl, lengths, row_bytes)
+    del k, v, kn, vn
+    return out
+
+
+def append_cpu_baseline(wl, lengths, row_bytes, budget_s: float = 3.0):
+    """The append oracle on a compact pool of the first requests: every
+    token of each request rewritten, as the bulk measurement does."""
+    import oracle.append_ref as append_ref
+    from paged_kv_decode_plan_gb300 import workloads
+    t = wl.table
+    k_all, v_all = workloads.as_codes(wl.k_pages), workloads.as_codes(wl.v_pages)
+    rng = np.random.default_rng(5)
+    tokens = 0
+    elapsed = 0.0
+    reqs = 0
+    for b in range(t.batch):
+        if elapsed >= budget_s:
+            break
+        pages = t.kv_indices[t.kv_indptr[b]: t.kv_indptr[b + 1]]
+        n = int(lengths[b])
+        if n == 0:
+            continue
+        k_pool, v_pool = k_all[pages], v_all[pages]
+        kn = rng.integers(0, 1 << 15, size=(n,) + k_pool.shape[2:], dtype=np.uint16)
+        vn = rng.integers(0, 1 << 15, size=(n,) + v_pool.shape[2:], dtype=np.uint16)
+        indptr = np.array([0, pages.size], np.int32)
+        indices = np.arange(pages.size, dtype=np.int32)
+        last = t.kv_last_page_len[b: b + 1]
+        t0 = time.perf_counter()
+        append_ref.append_kv(k_pool, v_pool, kn, vn, np.zeros(n, np.int32),
+                             np.arange(n, dtype=np.int32), indptr, indices, last)
+        elapsed += time.perf_counter() - t0
+        tokens += n
+        reqs += 1
+    moved = 2 * tokens * row_bytes * 2
+    return {"value": round(moved / elapsed / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "seconds": round(elapsed, 2),
+            "sample": "%d whole requests of the batch-64 pool (%d tokens), each in a "
+                      "compact pool of its own pages, plain Python loop" % (reqs, tokens)}
 
 
 def config_summary(line):
@@ -1080,6 +1245,9 @@ def run_reference(args, ranks):
     """The oracle as it stands, on the host cores, same metric and config."""
     import oracle
     from paged_kv_decode_plan_gb300 import workloads
+    if args.workload == "append":
+        raise SystemExit("--impl reference times the decode oracle; the append "
+                         "oracle's timing is the cpu_baseline of --workload append")
     oracle.build()
     wl = make_workload(args)
     codes = (workloads.as_codes(wl.q), workloads.as_codes(wl.k_pages),
@@ -1136,7 +1304,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["all"] + sorted(DESCRIPTIONS), default="all",
+    ap.add_argument("--workload", choices=["all", "append"] + sorted(DESCRIPTIONS),
+                    default="all",
                     help="all (default): every workload timed in one run, the "
                          "long-context batch as the headline line and the others "
                          "under per_config")
