@@ -82,7 +82,10 @@ typedef enum {
 /* Bits of the device status word (see pkd_check_status). */
 #define PKD_DEVICE_BAD_PAGE 1u    /* a page id outside [0, num_pages) */
 #define PKD_DEVICE_BAD_LENGTH 2u  /* a plan unit runs past the request */
-#define PKD_DEVICE_BAD_PLAN 4u    /* workspace does not hold a plan image */
+#define PKD_DEVICE_BAD_PLAN 4u    /* workspace does not hold a plan image for this
+                                     launch, or one of its units is malformed (a
+                                     request or slot out of range, a start off a
+                                     16-token tile boundary) */
 #define PKD_DEVICE_TIMEOUT 8u     /* a bounded pipeline wait ran out */
 /* Test hook: with the environment variable PKD_TEST_INJECT set to "no-loader"
  * or "no-consumers" when a decode kernel is launched, that role of every CTA
